@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the hot path on one GB300 (or N independent replicas under torchrun).
+
+A step is one pass of the convolution hot path over the 64,000-atom / ~2.56M-edge workload
+(128x0e+128x1o+128x2e, SH l<=3, outputs l<=3, fp32): spherical harmonics of the edge
+vectors, the fused convolution forward, and the sender-major convolution backward
+(dx, dy, dw). value = edges processed per second by all ranks (the "conv fwd+bwd edges/s"
+half of the metric). The tensor product on the 200,000-row workload is timed in the same
+run (forward and backward, own timed loops) and reported under "tp" (the "TP fwd achieved
+HBM GB/s" half). Inputs are resident in HBM; the edge weights alone (31.5 GB) exceed L2
+(129 MB), so no flush is needed between steps. "e2e" measures the same step through the
+public API with host buffers: pinned host -> device copies of the step's inputs and
+device -> host copies of all outputs inside the timed region.
+
+Throughput accounting follows "e3j ...", Sec. 3 Eq. (9): (bytes of inputs + outputs) /
+runtime, backward counting input primals, output cotangents and input cotangents.
+
+--impl reference times the float64 CPU oracle on the same workload (a bounded sample of
+receivers per step) on the host cores; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv fwd+bwd edges/s and TP fwd achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "edges/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "message_passing_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, units: float):
+    """Per-launch DRAM bytes of `kernel` from profiles/traffic.json, scaled to `units`
+    (edges or rows) of one launch; None when absent or taken on other kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            tr = json.load(f)
+    except Exception:
+        return None
+    ent = tr.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return float(ent["bytes_per_unit"]) * units
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic bytes (Eq. 9)
+# ---------------------------------------------------------------------------------------
+def conv_bytes(N, E, d1, d2, P, D, Nq, s):
+    fwd = N * d1 * Nq * s + E * d2 * s + E * P * Nq * s + (N + 1) * 4 + E * 4 + N * D * Nq * s
+    bwd = (N * d1 * Nq * s + E * d2 * s + E * P * Nq * s + N * D * Nq * s      # x, y, w, dm
+           + (N + 1) * 4 + 2 * E * 4                                           # sender-major index
+           + N * d1 * Nq * s + E * d2 * s + E * P * Nq * s)                    # dx, dy, dw
+    return fwd, bwd
+
+
+def sh_bytes(E, d2, s):
+    return E * 12 + E * d2 * s
+
+
+def tp_bytes(R, d1, d2, P, D, Nq, s):
+    fwd = R * (d1 * Nq + d2 + P * Nq + D * Nq) * s
+    bwd = R * (d1 * Nq + d2 + P * Nq + D * Nq + d1 * Nq + d2 + P * Nq) * s
+    return fwd, bwd
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------------------
+def oracle_conv_sample(w, g, ot, x, y, wfetch, dm, scale, n_recv, seed=0):
+    """Oracle conv fwd + bwd on the edges of n_recv receivers; returns (edges, seconds)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    recv = np.sort(rng.choice(g.n_nodes, size=n_recv, replace=False))
+    cnt = np.diff(g.rowptr)[recv]
+    edges = np.concatenate([np.arange(g.rowptr[r], g.rowptr[r + 1]) for r in recv]) if n_recv else np.zeros(0, int)
+    t0 = time.perf_counter()
+    oracle.conv_forward(ot, g.rowptr, g.sender, x, y, wfetch, scale, receivers=recv)
+    oracle.conv_backward_edges(ot, g.rowptr, g.sender, x, y, wfetch, dm, scale, edges=edges)
+    oracle.conv_backward_dx(ot, g.rowptr, g.sender, y, wfetch, dm, scale, senders=recv, Nq=w.mul)
+    return int(cnt.sum()), time.perf_counter() - t0
+
+
+def cpu_inputs(w, g, ot):
+    import oracle
+    from synth import workloads as W
+    x, _ = W.make_conv(w, g, ot.n_paths, edge_ids=np.zeros(0, np.int64))
+    y = oracle.sh(g.vec.astype(np.float32).astype(np.float64), w.sh_lmax)
+    return x.astype(np.float64), y
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores, on the benchmark workload."""
+    import oracle
+    from synth import STREAM_GRAD
+    from synth import workloads as W
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    oracle.build()
+    w = W.WORKLOADS[4]
+    ot = oracle.table(w.blocks, w.sh_lmax, w.out_lmax)
+    g = W.make_graph(w, n_atoms=args.atoms, order=args.order)
+    scale = g.n_nodes / g.n_edges
+    wfetch = lambda ids: W.make_conv(w, g, ot.n_paths, edge_ids=np.asarray(ids, np.int64))[1]
+    x, y = cpu_inputs(w, g, ot)
+    dm = W.make_grad(w, g.n_nodes, ot.D).astype(np.float64)
+    n_recv = args.ref_receivers
+    for _ in range(args.warmup):
+        oracle_conv_sample(w, g, ot, x, y, wfetch, dm, scale, n_recv, seed=1)
+    tot_e, tot_t = 0, 0.0
+    for k in range(args.steps):
+        e, t = oracle_conv_sample(w, g, ot, x, y, wfetch, dm, scale, n_recv, seed=100 + k)
+        tot_e += e
+        tot_t += t
+    v = tot_e / tot_t
+    cores = oracle.num_threads()
+    sample = f"{n_recv} random receivers per step ({tot_e / args.steps:.0f} edges): conv fwd + dy/dw of their edges + dx of {n_recv} senders"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, g, args),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, g, args):
+    return {"workload": f"{w.name} ({args.dtype})", "atoms": g.n_nodes, "edges": g.n_edges,
+            "atom_order": args.order, "parallelism": "replicas" if args.gpus > 1 else "single",
+            "l2": "inputs larger than L2 (edge weights alone exceed 129 MB)",
+            "tp_workload": "tp-batched: 200000 rows, 128x0e+128x1o+128x2e, SH l<=3, out l<=3 (fp32)"}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import message_passing_gb300 as e3
+    from message_passing_gb300 import build as libbuild
+    from synth import STREAM_GRAD, STREAM_W, device_normal
+    from synth import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(e3.LIB_PATH):
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    e3.load()
+    bf16 = args.dtype == "bf16"
+    dt = torch.bfloat16 if bf16 else torch.float32
+    s = 2 if bf16 else 4
+    hbm_peak, peak_kind = peaks()
+
+    # ---- conv workload
+    w = W.WORKLOADS[4]
+    t = e3.Table.create(w.blocks, w.mul, w.sh_lmax, w.out_lmax)
+    g = W.make_graph(w, n_atoms=args.atoms, order=args.order)
+    N, E, Nq, P, D = g.n_nodes, g.n_edges, w.mul, t.n_paths, t.D
+    scale = N / E
+    x_np, _ = W.make_conv(w, g, P, edge_ids=np.zeros(0, np.int64))
+    vec = torch.from_numpy(g.vec.astype(np.float32)).to(dev)
+    rp = torch.from_numpy(g.rowptr).to(dev)
+    sd = torch.from_numpy(g.sender).to(dev)
+    xd = torch.from_numpy(x_np).to(dev).to(dt)
+    wd = device_normal((E, P, Nq), (w.wid, STREAM_W), W.weight_scale(w, P), device=dev, dtype=dt)
+    dmd = device_normal((N, D, Nq), (w.wid, STREAM_GRAD), device=dev, dtype=dt)
+    y = torch.empty((E, t.d2), device=dev, dtype=dt)
+    m = torch.empty((N, D, Nq), device=dev, dtype=dt)
+    dx, dy, dw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+    csc = e3.graph_prepare(rp, sd, N)
+    e3.check_device_status()
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        e3.sh_forward(vec, w.sh_lmax, out=y, stream=stream)
+        if ev: ev[1].record(stream)
+        e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream)
+        if ev: ev[2].record(stream)
+        e3.conv_backward(t, csc, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream)
+        if ev: ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e3.check_device_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local) if rank == 0 else None
+    if clocks: clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    elapsed = t0.elapsed_time(t1) / 1e3
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    ksh = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    kfw = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    kbw = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    e3.check_device_status()
+    bf, bb = conv_bytes(N, E, t.d1, t.d2, P, D, Nq, s)
+    bsh = sh_bytes(E, t.d2, s)
+    rows = {
+        "sh": {"ms": ksh * 1e3, "alg_GBps": bsh / ksh / 1e9, "frac": bsh / ksh / 1e9 / hbm_peak},
+        "conv_fwd": {"ms": kfw * 1e3, "alg_GBps": bf / kfw / 1e9, "frac": bf / kfw / 1e9 / hbm_peak,
+                     "edges_per_s": E / kfw},
+        "conv_bwd": {"ms": kbw * 1e3, "alg_GBps": bb / kbw / 1e9, "frac": bb / kbw / 1e9 / hbm_peak,
+                     "edges_per_s": E / kbw},
+    }
+    dom = max(("conv_fwd", kfw, bf), ("conv_bwd", kbw, bb), key=lambda r: r[1])
+    traffic = ncu_traffic(dom[0], E)
+    roofline = {"kernel": dom[0], "bound": "hbm", "achieved": dom[2] / dom[1] / 1e9, "peak": hbm_peak,
+                "unit": "GB/s", "frac": dom[2] / dom[1] / 1e9 / hbm_peak, "traffic": traffic,
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"}
+
+    # ---- TP rows
+    tp = None
+    if not args.no_tp:
+        del dw, dy, dx
+        torch.cuda.empty_cache()
+        w2 = W.WORKLOADS[2]
+        t2 = e3.Table.create(w2.blocks, w2.mul, w2.sh_lmax, w2.out_lmax)
+        R = w2.rows if args.tp_rows is None else args.tp_rows
+        u, x2, ww2 = W.make_tp(w2, t2.n_paths, rows=R)
+        v2 = torch.from_numpy(u.astype(np.float32)).to(dev)
+        x2d = torch.from_numpy(x2).to(dev)
+        w2d = torch.from_numpy(ww2).to(dev)
+        dz = device_normal((R, t2.D, w2.mul), (w2.wid, STREAM_GRAD), device=dev)
+        y2 = e3.sh_forward(v2, w2.sh_lmax)
+        z = torch.empty((R, t2.D, w2.mul), device=dev)
+        gx, gy, gw = torch.empty_like(x2d), torch.empty_like(y2), torch.empty_like(w2d)
+        reps = max(args.steps, 5)
+        for _ in range(args.warmup):
+            e3.tp_forward(t2, x2d, y2, w2d, out=z, stream=stream)
+            e3.tp_backward(t2, x2d, y2, w2d, dz, out=(gx, gy, gw), stream=stream)
+        torch.cuda.synchronize()
+        ef = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for k in range(reps):
+            ef[k][0].record(stream)
+            e3.tp_forward(t2, x2d, y2, w2d, out=z, stream=stream)
+            ef[k][1].record(stream)
+            e3.tp_backward(t2, x2d, y2, w2d, dz, out=(gx, gy, gw), stream=stream)
+            ef[k][2].record(stream)
+        torch.cuda.synchronize()
+        tf = statistics.mean(e[0].elapsed_time(e[1]) for e in ef) / 1e3
+        tb = statistics.mean(e[1].elapsed_time(e[2]) for e in ef) / 1e3
+        btf, btb = tp_bytes(R, t2.d1, t2.d2, t2.n_paths, t2.D, w2.mul, 4)
+        tp = {"rows": R, "fwd": {"ms": tf * 1e3, "alg_GBps": btf / tf / 1e9, "frac": btf / tf / 1e9 / hbm_peak,
+                                 "rows_per_s": R / tf, "traffic": ncu_traffic("tp_fwd", R)},
+              "bwd": {"ms": tb * 1e3, "alg_GBps": btb / tb / 1e9, "frac": btb / tb / 1e9 / hbm_peak,
+                      "rows_per_s": R / tb}}
+        del x2d, w2d, dz, y2, z, gx, gy, gw
+        torch.cuda.empty_cache()
+        dx, dy, dw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+
+    # ---- end to end through the API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda tns: torch.empty(tns.shape, dtype=tns.dtype, pin_memory=True).copy_(tns)
+        h_vec, h_rp, h_sd, h_x = pin(vec.cpu()), pin(rp.cpu()), pin(sd.cpu()), pin(xd.cpu())
+        h_w = torch.empty(wd.shape, dtype=wd.dtype, pin_memory=True)
+        h_w.copy_(wd)
+        h_dm = pin(dmd.cpu())
+        o_m = torch.empty(m.shape, dtype=dt, pin_memory=True)
+        o_dx = torch.empty(xd.shape, dtype=dt, pin_memory=True)
+        o_dy = torch.empty(y.shape, dtype=dt, pin_memory=True)
+        o_dw = torch.empty(wd.shape, dtype=dt, pin_memory=True)
+        h2d = sum(a.numel() * a.element_size() for a in (h_vec, h_rp, h_sd, h_x, h_w, h_dm))
+        d2h = sum(a.numel() * a.element_size() for a in (o_m, o_dx, o_dy, o_dw))
+
+        def e2e_step():
+            vec.copy_(h_vec, non_blocking=True); rp.copy_(h_rp, non_blocking=True)
+            sd.copy_(h_sd, non_blocking=True); xd.copy_(h_x, non_blocking=True)
+            wd.copy_(h_w, non_blocking=True); dmd.copy_(h_dm, non_blocking=True)
+            e3.sh_forward(vec, w.sh_lmax, out=y, stream=stream)
+            c = e3.graph_prepare(rp, sd, N, out=csc, stream=stream)
+            e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream)
+            e3.conv_backward(t, c, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream)
+            o_m.copy_(m, non_blocking=True); o_dx.copy_(dx, non_blocking=True)
+            o_dy.copy_(dy, non_blocking=True); o_dw.copy_(dw, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        ke = max(1, min(args.steps, args.e2e_steps))
+        if world > 1:
+            dist.barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        te = a0.elapsed_time(a1) / 1e3
+        if world > 1:
+            tt = torch.tensor([te], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e3.check_device_status()
+        e2e = {"value": E * ke * world / te, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": ke, "ms_per_step": te / ke * 1e3,
+               "includes": "pinned H2D of vec, rowptr, sender, x, w, dm; SH; graph_prepare; conv fwd; conv bwd; D2H of m, dx, dy, dw"}
+        del h_w, o_dw
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        from synth import STREAM_GRAD as SG
+        ot = oracle.table(w.blocks, w.sh_lmax, w.out_lmax)
+        wfetch = lambda ids: wd[torch.from_numpy(np.asarray(ids, np.int64)).to(dev)].float().cpu().numpy().astype(np.float64)
+        xo = xd.float().cpu().numpy().astype(np.float64)
+        yo = oracle.sh(g.vec.astype(np.float32).astype(np.float64), w.sh_lmax)
+        dmo = dmd.float().cpu().numpy().astype(np.float64)
+        n_recv = 8
+        e_cnt, secs = oracle_conv_sample(w, g, ot, xo, yo, wfetch, dmo, scale, n_recv, seed=5)
+        # grow the sample to about 10 s of CPU work
+        n_recv = int(min(N, max(8, n_recv * 10.0 / max(secs, 1e-3))))
+        e_cnt, secs = oracle_conv_sample(w, g, ot, xo, yo, wfetch, dmo, scale, n_recv, seed=6)
+        cpu = {"value": e_cnt / secs, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{n_recv} random receivers ({e_cnt} edges): oracle conv fwd + dy/dw of those edges + dx of {n_recv} senders, f64, {secs:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": E * args.steps * world / elapsed, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if bf16 else "f32", "data": "synthetic", "config": workload_config(w, g, args),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps,
+                "clocks": clk, "rows": rows, "tp": tp}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--order", choices=["cell", "draw"], default="cell")
+    ap.add_argument("--atoms", type=int, default=None, help="smaller conv workload (profiling)")
+    ap.add_argument("--tp-rows", type=int, default=None, help="smaller TP workload (profiling)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--ref-receivers", type=int, default=24)
+    ap.add_argument("--no-tp", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * e3gb: channelwise Clebsch-Gordan tensor product and message-passing convolution on
+ * NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * The operations are those of "e3j: An efficient and open-source backend for Euclidean
+ * equivariant operations on GPU and TPU" (arXiv HTML version), App. E.1:
+ *   - Eq. (10)-(11): tensor product of l.h.s. features x with r.h.s. features y (real
+ *     spherical harmonics, no channel axis), weighted per path and channel;
+ *   - Eq. (12)-(13): message-passing convolution, the same product per edge with the sender's
+ *     x, summed at the receiver over a receiver-sorted CSR edge list;
+ *   - Eq. (15)-(16): their reverse-mode (VJP) rules.
+ * Spherical harmonics: App. A.3 Eq. (4) and App. G.1. CG coefficients: App. G.2.
+ *
+ * Layouts (all row-major, channel axis innermost: "trailing channels", App. E.2.1):
+ *   x  [rows or nodes][d1][Nq]   d1 = sum over x irreps blocks of (2l+1), blocks in the order
+ *                                given to e3gb_table_create, m = -l..l inside a block
+ *   y  [rows or edges][d2]       d2 = (sh_lmax+1)^2, Y_0, Y_1, ... concatenated
+ *   w  [rows or edges][P][Nq]    P paths in table order
+ *   z, m, dz, dm [rows or nodes][D][Nq]
+ * Nq (the uniform multiplicity) must be 4, 8, 16, 32, 64 or 128.
+ *
+ * Memory and streams: every device buffer belongs to the caller; no call allocates device
+ * memory. Work is enqueued on the caller's stream (a cudaStream_t passed as void*, NULL =
+ * legacy default stream) and the call returns without synchronising. Device pointers must
+ * be 16-byte aligned (fp32) or 8-byte aligned (bf16) and must not alias each other.
+ * Outputs are overwritten, never accumulated into.
+ *
+ * Errors: each call checks its arguments on the host and returns a status; the message of
+ * the last failure on the calling thread is e3gb_last_error(). Index errors found on the
+ * device (a sender or receiver outside [0, n_nodes), a decreasing or out-of-range CSR
+ * pointer) never fault: the offending edge or segment is skipped and a device error word
+ * is set; e3gb_check_device_status() reads and clears it.
+ *
+ * Determinism: for identical inputs and launch configuration results are bitwise identical
+ * from run to run (fixed summation order, no floating-point atomics).
+ */
+#ifndef E3GB_H
+#define E3GB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    E3GB_OK = 0,
+    E3GB_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad dtype */
+    E3GB_ERR_UNSUPPORTED = 2,   /* irreps configuration or channel count not built in */
+    E3GB_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+    E3GB_ERR_BAD_GRAPH = 4,     /* CSR arrays inconsistent on the host side */
+    E3GB_ERR_DEVICE_INDEX = 5   /* the device saw an out-of-range index (see above) */
+} e3gb_status;
+
+typedef enum {
+    E3GB_F32 = 0,   /* fp32 storage, fp32 arithmetic */
+    E3GB_BF16 = 1   /* bf16 storage of x, y, w, dz/dm and all outputs; fp32 accumulation,
+                       outputs rounded to nearest even once */
+} e3gb_dtype;
+
+/* Irreps of x with a uniform multiplicity: n blocks, block i of degree l[i] in 0..3 and
+ * parity parity[i] = +1 (even) or -1 (odd), each with mul channels. */
+typedef struct {
+    int32_t n;
+    const int32_t *l;
+    const int32_t *parity;
+    int32_t mul;
+} e3gb_irreps;
+
+/* Opaque path table: the paths (x block, l2, l3) with their real CG blocks, baked into the
+ * kernels at compile time for each supported configuration. Host-owned. */
+typedef struct e3gb_table e3gb_table;
+
+/* table_create flags */
+#define E3GB_PATHS_SUMMED 0    /* one output block per distinct (l3, p3); default */
+#define E3GB_PATHS_SEPARATE 1  /* one output block per path */
+
+/* Build the path table for x irreps, SH degrees 0..sh_lmax and output degrees <= out_lmax
+ * (App. A.3 Eq. 6: every l3 in |l1-l2|..l1+l2; App. B.1: output parity p1 (-1)^l2).
+ * Paths are ordered by (x block, l2, l3). In summed mode the output blocks are the distinct
+ * (l3, p3) ordered by l3 with the natural parity (-1)^l3 first.
+ * Returns E3GB_ERR_UNSUPPORTED when the configuration has no compiled kernels
+ * (e3gb_config_count / e3gb_config_describe list the built ones). *out is set on success
+ * and must be released with e3gb_table_destroy. */
+e3gb_status e3gb_table_create(const e3gb_irreps *x, int32_t sh_lmax, int32_t out_lmax,
+                              int32_t flags, e3gb_table **out);
+e3gb_status e3gb_table_destroy(e3gb_table *t);
+
+/* Sizes of a table; any output pointer may be NULL. nnz = number of nonzero CG records. */
+e3gb_status e3gb_table_info(const e3gb_table *t, int32_t *d1, int32_t *d2, int32_t *n_paths,
+                            int32_t *D, int32_t *nnz, int32_t *mul);
+
+/* Path descriptors, n_paths x 8 int32: x block, l1, p1, l2, l3, p3, output block, output
+ * offset. NULL-safe sizes: paths must hold 8*n_paths ints. */
+e3gb_status e3gb_table_paths(const e3gb_table *t, int32_t *paths);
+
+/* CG records, nnz x 5 doubles: path, m1, m2, m3 (0-based, i.e. m + l), value (App. G.2
+ * normalisation sum_{m1,m2} C^2 = 1 per m3; first row-major entry of each block > 0). */
+e3gb_status e3gb_table_coefficients(const e3gb_table *t, double *records);
+
+/* Built configurations: count, and for index i the x irreps (up to 8 blocks), sh_lmax,
+ * out_lmax and flags. */
+int32_t e3gb_config_count(void);
+e3gb_status e3gb_config_describe(int32_t i, int32_t *n_blocks, int32_t *l, int32_t *parity,
+                                 int32_t *sh_lmax, int32_t *out_lmax, int32_t *flags);
+
+/* Real spherical harmonics (App. A.3 Eq. 4, App. G.1): y[e] = (Y_l(u_e))_{l=0..lmax},
+ * u_e = vec[e]/|vec[e]| (u = 0 when |vec| < 1e-12, giving Y_0 = 1 and Y_l>0 = 0),
+ * component normalisation sum_m Y_lm^2 = 2l+1, l = 1 ordered sqrt(3)(y, z, x).
+ * vec: device fp32 [n, 3]; y: device [n, (lmax+1)^2] of dtype. lmax in 0..3. */
+e3gb_status e3gb_sh_forward(int32_t lmax, int64_t n, const float *vec, void *y,
+                            e3gb_dtype dtype, void *stream);
+
+/* Tensor product on rows (Eq. 10-11): z[r] = sum_p w[r,p] * C_p(x[r], y[r]) into the
+ * output block of path p. x [rows,d1,Nq], y [rows,d2], w [rows,P,Nq], z [rows,D,Nq]. */
+e3gb_status e3gb_tp_forward(const e3gb_table *t, int64_t rows, const void *x, const void *y,
+                            const void *w, void *z, e3gb_dtype dtype, void *stream);
+
+/* Its VJP (Eq. 15 with the weights as a third operand): from dz [rows,D,Nq] computes
+ * dx [rows,d1,Nq], dy [rows,d2] (summed over channels) and dw [rows,P,Nq] in one pass that
+ * reads dz once. */
+e3gb_status e3gb_tp_backward(const e3gb_table *t, int64_t rows, const void *x, const void *y,
+                             const void *w, const void *dz, void *dx, void *dy, void *dw,
+                             e3gb_dtype dtype, void *stream);
+
+/* Workspace (bytes) that e3gb_graph_prepare needs for n_nodes nodes. */
+size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes);
+
+/* Sender-major index of a receiver-sorted CSR graph (rowptr [n_nodes+1], sender [n_edges],
+ * receiver b owns edges [rowptr[b], rowptr[b+1])). Writes csc_ptr [n_nodes+1], and for the
+ * k-th edge in sender order csc_edge[k] (its CSR edge id) and csc_recv[k] (its receiver);
+ * edges of one sender keep increasing edge id (stable). Used by the backward convolution to
+ * sum dx per sender without atomics (the transposed graph of Eq. 16). All arrays are
+ * device arrays. A sender outside [0, n_nodes) is left out of the index and flagged in the
+ * device error word. workspace: device memory of at least
+ * e3gb_graph_prepare_workspace_bytes(n_nodes) bytes, 16-byte aligned; its contents on entry
+ * do not matter. */
+e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t *rowptr,
+                               const int32_t *sender, int32_t *csc_ptr, int32_t *csc_edge,
+                               int32_t *csc_recv, void *workspace, size_t ws_bytes,
+                               void *stream);
+
+/* Message-passing convolution (Eq. 12-13): for every receiver b,
+ *   m[b] = scale * sum_{e in [rowptr[b], rowptr[b+1])} TP(x[sender[e]], y[e], w[e]),
+ * accumulated in a fixed order in registers, written once (receivers without edges get 0).
+ * x [n_nodes,d1,Nq], y [n_edges,d2], w [n_edges,P,Nq], m [n_nodes,D,Nq]. */
+e3gb_status e3gb_conv_forward(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                              const int32_t *rowptr, const int32_t *sender, const void *x,
+                              const void *y, const void *w, float scale, void *m,
+                              e3gb_dtype dtype, void *stream);
+
+/* Its VJP (Eq. 16) from dm [n_nodes,D,Nq]:
+ *   dw[e,p] = scale * sum_m3 dm[b][blk p, m3] * (C_p(x[a], y[e]))[m3],
+ *   dy[e]   = scale * sum over paths and channels of the x, w, dm couplings,
+ *   dx[a]   = scale * sum over the edges of sender a of the y, w, dm couplings,
+ * walking the graph in sender order (csc_* from e3gb_graph_prepare) so that dx[a] is summed
+ * in registers in a fixed order: deterministic, no atomics, no workspace.
+ * dx [n_nodes,d1,Nq], dy [n_edges,d2], dw [n_edges,P,Nq]. */
+e3gb_status e3gb_conv_backward(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                               const int32_t *csc_ptr, const int32_t *csc_edge,
+                               const int32_t *csc_recv, const void *x, const void *y,
+                               const void *w, const void *dm, float scale, void *dx, void *dy,
+                               void *dw, e3gb_dtype dtype, void *stream);
+
+/* Synchronise stream, read and clear the device error word of the current device.
+ * E3GB_OK when clean, E3GB_ERR_DEVICE_INDEX when a kernel skipped bad indices (*flags, if
+ * not NULL, receives the bits: 1 bad sender, 2 bad CSR pointer, 4 bad receiver / edge id). */
+e3gb_status e3gb_check_device_status(void *stream, int32_t *flags);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *e3gb_last_error(void);
+
+/* Library version string. */
+const char *e3gb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* E3GB_H */

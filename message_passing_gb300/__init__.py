@@ -1,0 +1,273 @@
+"""Python binding of libe3gb.so (include/e3gb.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; PyTorch provides device
+memory and streams. The functions keep the C names without the ``e3gb_`` prefix and take
+torch tensors. If the library is missing or fails to load, importing the functions raises
+(there is no CPU path).
+
+Operations follow "e3j: An efficient and open-source backend for Euclidean equivariant
+operations on GPU and TPU", App. E.1 Eq. (10)-(16); see include/e3gb.h for layouts.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libe3gb.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BAD_GRAPH, ERR_DEVICE_INDEX = range(6)
+F32, BF16 = 0, 1
+PATHS_SUMMED, PATHS_SEPARATE = 0, 1
+
+# every symbol include/e3gb.h declares
+SYMBOLS = (
+    "e3gb_table_create", "e3gb_table_destroy", "e3gb_table_info", "e3gb_table_paths",
+    "e3gb_table_coefficients", "e3gb_config_count", "e3gb_config_describe", "e3gb_sh_forward",
+    "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
+    "e3gb_graph_prepare", "e3gb_conv_forward", "e3gb_conv_backward",
+    "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
+)
+
+
+class E3GBError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"e3gb status {status}: {msg}")
+        self.status = status
+
+
+class _Irreps(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("l", ctypes.POINTER(ctypes.c_int32)),
+                ("parity", ctypes.POINTER(ctypes.c_int32)), ("mul", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libe3gb.so (built by message_passing_gb300.build). Raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with message_passing_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    i32, i64, vp, f32, szt = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+    P32 = ctypes.POINTER(ctypes.c_int32)
+    sig = {
+        "e3gb_table_create": (i32, [ctypes.POINTER(_Irreps), i32, i32, i32, ctypes.POINTER(vp)]),
+        "e3gb_table_destroy": (i32, [vp]),
+        "e3gb_table_info": (i32, [vp, P32, P32, P32, P32, P32, P32]),
+        "e3gb_table_paths": (i32, [vp, P32]),
+        "e3gb_table_coefficients": (i32, [vp, ctypes.POINTER(ctypes.c_double)]),
+        "e3gb_config_count": (i32, []),
+        "e3gb_config_describe": (i32, [i32, P32, P32, P32, P32, P32, P32]),
+        "e3gb_sh_forward": (i32, [i32, i64, vp, vp, i32, vp]),
+        "e3gb_tp_forward": (i32, [vp, i64, vp, vp, vp, vp, i32, vp]),
+        "e3gb_tp_backward": (i32, [vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp]),
+        "e3gb_graph_prepare_workspace_bytes": (szt, [i64]),
+        "e3gb_graph_prepare": (i32, [i64, i64, vp, vp, vp, vp, vp, vp, szt, vp]),
+        "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, vp, i32, vp]),
+        "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, i32, vp]),
+        "e3gb_check_device_status": (i32, [vp, P32]),
+        "e3gb_last_error": (ctypes.c_char_p, []),
+        "e3gb_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise E3GBError(status, load().e3gb_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(*ts):
+    import torch
+    dt = {t.dtype for t in ts if t is not None}
+    if dt == {torch.float32}:
+        return F32
+    if dt == {torch.bfloat16}:
+        return BF16
+    raise TypeError(f"tensors must all be float32 or all bfloat16, got {dt}")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def version() -> str:
+    return load().e3gb_version().decode()
+
+
+def configs() -> list[dict]:
+    """The irreps configurations compiled into the library."""
+    lib = load()
+    out = []
+    for i in range(lib.e3gb_config_count()):
+        n = ctypes.c_int32()
+        l = (ctypes.c_int32 * 8)()
+        p = (ctypes.c_int32 * 8)()
+        a, b, f = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.e3gb_config_describe(i, ctypes.byref(n), l, p, ctypes.byref(a), ctypes.byref(b), ctypes.byref(f)))
+        out.append({"blocks": [(l[k], p[k]) for k in range(n.value)], "sh_lmax": a.value,
+                    "out_lmax": b.value, "per_path": bool(f.value)})
+    return out
+
+
+@dataclass
+class Table:
+    """Path table handle (e3gb_table). blocks: [(l, parity)] of x; mul: channels."""
+    handle: ctypes.c_void_p
+    blocks: list
+    mul: int
+    sh_lmax: int
+    out_lmax: int
+    per_path: bool
+    d1: int = 0
+    d2: int = 0
+    n_paths: int = 0
+    D: int = 0
+    nnz: int = 0
+
+    @classmethod
+    def create(cls, blocks, mul: int, sh_lmax: int, out_lmax: int, per_path: bool = False) -> "Table":
+        lib = load()
+        n = len(blocks)
+        L = (ctypes.c_int32 * max(1, n))(*[b[0] for b in blocks])
+        P = (ctypes.c_int32 * max(1, n))(*[b[1] for b in blocks])
+        ir = _Irreps(n, L, P, mul)
+        h = ctypes.c_void_p()
+        _check(lib.e3gb_table_create(ctypes.byref(ir), sh_lmax, out_lmax,
+                                     PATHS_SEPARATE if per_path else PATHS_SUMMED, ctypes.byref(h)))
+        t = cls(h, list(blocks), mul, sh_lmax, out_lmax, per_path)
+        v = [ctypes.c_int32() for _ in range(6)]
+        _check(lib.e3gb_table_info(h, *[ctypes.byref(x) for x in v]))
+        t.d1, t.d2, t.n_paths, t.D, t.nnz, _ = (x.value for x in v)
+        return t
+
+    def paths(self) -> list[tuple]:
+        buf = (ctypes.c_int32 * (8 * self.n_paths))()
+        _check(load().e3gb_table_paths(self.handle, buf))
+        return [tuple(buf[8 * i:8 * i + 8]) for i in range(self.n_paths)]
+
+    def coefficients(self):
+        import numpy as np
+        buf = (ctypes.c_double * (5 * self.nnz))()
+        _check(load().e3gb_table_coefficients(self.handle, buf))
+        return np.frombuffer(buf, dtype=np.float64).reshape(self.nnz, 5).copy()
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.e3gb_table_destroy(h)
+            self.handle = None
+
+
+def sh_forward(vec, lmax: int, out=None, dtype=None, stream=None):
+    """y[n, (lmax+1)^2] = real SH of vec[n, 3] (fp32 device tensor)."""
+    import torch
+    _contig(vec)
+    if vec.dtype != torch.float32:
+        raise TypeError("vec must be float32")
+    dt = dtype or torch.float32
+    y = out if out is not None else torch.empty((vec.shape[0], (lmax + 1) ** 2), dtype=dt, device=vec.device)
+    _check(load().e3gb_sh_forward(lmax, vec.shape[0], _ptr(vec), _ptr(y), _dtype(y), _stream(stream)))
+    return y
+
+
+def tp_forward(t: Table, x, y, w, out=None, stream=None):
+    import torch
+    _contig(x, y, w, out)
+    z = out if out is not None else torch.empty((x.shape[0], t.D, t.mul), dtype=x.dtype, device=x.device)
+    _check(load().e3gb_tp_forward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(z),
+                                  _dtype(x, y, w, z), _stream(stream)))
+    return z
+
+
+def tp_backward(t: Table, x, y, w, dz, out=None, stream=None):
+    import torch
+    _contig(x, y, w, dz)
+    if out is None:
+        out = (torch.empty_like(x), torch.empty_like(y), torch.empty_like(w))
+    dx, dy, dw = out
+    _check(load().e3gb_tp_backward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(dz), _ptr(dx),
+                                   _ptr(dy), _ptr(dw), _dtype(x, y, w, dz, dx, dy, dw), _stream(stream)))
+    return dx, dy, dw
+
+
+def graph_prepare_workspace_bytes(n_nodes: int) -> int:
+    return int(load().e3gb_graph_prepare_workspace_bytes(n_nodes))
+
+
+def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream=None):
+    """(csc_ptr, csc_edge, csc_recv) int32 device tensors."""
+    import torch
+    _contig(rowptr, sender)
+    E = sender.shape[0]
+    dev = rowptr.device
+    if out is None:
+        out = (torch.empty(n_nodes + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(E, 1), dtype=torch.int32, device=dev),
+               torch.empty(max(E, 1), dtype=torch.int32, device=dev))
+    nb = graph_prepare_workspace_bytes(n_nodes)
+    ws = workspace if workspace is not None else torch.empty(nb, dtype=torch.uint8, device=dev)
+    cp, ce, cr = out
+    _check(load().e3gb_graph_prepare(n_nodes, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(cp),
+                                     _ptr(ce) if E else None, _ptr(cr) if E else None, _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)))
+    return cp, ce, cr
+
+
+def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stream=None):
+    import torch
+    _contig(rowptr, sender, x, y, w)
+    N, E = x.shape[0], sender.shape[0]
+    m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=x.dtype, device=x.device)
+    _check(load().e3gb_conv_forward(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
+                                    _ptr(y) if E else None, _ptr(w) if E else None, float(scale), _ptr(m),
+                                    _dtype(x, m, *( (y, w) if E else ())), _stream(stream)))
+    return m
+
+
+def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=None):
+    """csc = graph_prepare(...) output. Returns (dx, dy, dw)."""
+    import torch
+    cp, ce, cr = csc
+    _contig(x, y, w, dm)
+    N, E = x.shape[0], y.shape[0]
+    if out is None:
+        out = (torch.empty_like(x), torch.empty_like(y), torch.empty_like(w))
+    dx, dy, dw = out
+    _check(load().e3gb_conv_backward(t.handle, N, E, _ptr(cp), _ptr(ce) if E else None, _ptr(cr) if E else None,
+                                     _ptr(x), _ptr(y) if E else None, _ptr(w) if E else None, _ptr(dm),
+                                     float(scale), _ptr(dx), _ptr(dy) if E else None, _ptr(dw) if E else None,
+                                     _dtype(x, dm, dx, *((y, w, dy, dw) if E else ())), _stream(stream)))
+    return dx, dy, dw
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise and read/clear the device error word; raises E3GBError if it was set."""
+    flags = ctypes.c_int32()
+    st = load().e3gb_check_device_status(_stream(stream), ctypes.byref(flags))
+    if st != OK:
+        raise E3GBError(st, load().e3gb_last_error().decode())
+    return flags.value

@@ -1,0 +1,380 @@
+// C ABI of the library (include/e3gb.h): argument checks, table objects, dispatch to the
+// per-configuration kernels, and the device error word.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/e3gb.h"
+#include "kernels.cuh"
+
+namespace e3gb {
+#define E3GB_CONFIG(ID, XC, L2, L3, PP) const ConfigOps* ops_##ID();
+#include "configs.def"
+#undef E3GB_CONFIG
+
+static const ConfigOps* (*const kRegistry[])() = {
+#define E3GB_CONFIG(ID, XC, L2, L3, PP) ops_##ID,
+#include "configs.def"
+#undef E3GB_CONFIG
+};
+constexpr int kNumConfigs = int(sizeof(kRegistry) / sizeof(kRegistry[0]));
+
+cudaError_t sh_forward(int lmax, int64_t n, const float* vec, void* y, int bf16, cudaStream_t s);
+size_t graph_workspace_bytes(int64_t N);
+cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
+                          int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------
+// launch sizing: grid = min(blocks needed, resident blocks per SM x SMs), cached per kernel
+// ------------------------------------------------------------------------------------------
+int grid_for(const void* kernel, int block, int64_t per_block, int64_t units) {
+    if (units <= 0) return 0;
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> resident;  // blocks per device, by kernel
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int cap = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        const std::pair<const void*, int> key(kernel, dev);
+        auto it = resident.find(key);
+        if (it == resident.end()) {
+            int per_sm = 0, sms = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, 0);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cap = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+            resident.emplace(key, cap);
+        } else {
+            cap = it->second;
+        }
+    }
+    const int64_t need = (units + per_block - 1) / per_block;
+    return int(need < cap ? need : cap);
+}
+}  // namespace e3gb
+
+using namespace e3gb;
+
+// the device error word (one per device that loads the library)
+__device__ unsigned e3gb_device_error_word;
+
+struct e3gb_table {
+    const ConfigOps* ops;
+    int cfg;
+    int mul;
+};
+
+namespace {
+thread_local std::string g_last_error;
+
+e3gb_status fail(e3gb_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+e3gb_status ok() { return E3GB_OK; }
+
+e3gb_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return E3GB_OK;
+    return fail(E3GB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// device address of the error word for the current device (cached per device)
+unsigned* error_word(e3gb_status* st) {
+    static std::mutex mu;
+    static std::unordered_map<int, unsigned*> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_status(e, "cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, e3gb_device_error_word);
+    if (e != cudaSuccess) {
+        *st = cuda_status(e, "cudaGetSymbolAddress(error word)");
+        return nullptr;
+    }
+    addr.emplace(dev, static_cast<unsigned*>(p));
+    return static_cast<unsigned*>(p);
+}
+
+bool valid_mul(int mul) { return mul == 4 || mul == 8 || mul == 16 || mul == 32 || mul == 64 || mul == 128; }
+
+// a pointer must be device-accessible memory of this process, aligned as required
+e3gb_status check_ptr(const void* p, const char* name, size_t align, bool needed) {
+    if (!needed) return E3GB_OK;
+    if (p == nullptr) return fail(E3GB_ERR_INVALID_ARG, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % align != 0)
+        return fail(E3GB_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(E3GB_ERR_INVALID_ARG, "%s: cannot query pointer (%s)", name, cudaGetErrorString(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(E3GB_ERR_INVALID_ARG, "%s is not device memory", name);
+    return E3GB_OK;
+}
+
+size_t elt_bytes(e3gb_dtype d) { return d == E3GB_BF16 ? 2 : 4; }
+size_t vec_align(e3gb_dtype d) { return d == E3GB_BF16 ? 8 : 16; }
+
+e3gb_status check_table(const e3gb_table* t, e3gb_dtype dtype) {
+    if (t == nullptr || t->ops == nullptr) return fail(E3GB_ERR_INVALID_ARG, "table is NULL");
+    if (dtype != E3GB_F32 && dtype != E3GB_BF16) return fail(E3GB_ERR_INVALID_ARG, "unknown dtype %d", int(dtype));
+    return E3GB_OK;
+}
+
+#define E3GB_TRY(expr)                       \
+    do {                                     \
+        const e3gb_status _s = (expr);       \
+        if (_s != E3GB_OK) return _s;        \
+    } while (0)
+}  // namespace
+
+extern "C" {
+
+const char* e3gb_last_error(void) { return g_last_error.c_str(); }
+const char* e3gb_version(void) { return "e3gb 0.1.0 (sm_103a)"; }
+
+int32_t e3gb_config_count(void) { return kNumConfigs; }
+
+e3gb_status e3gb_config_describe(int32_t i, int32_t* n_blocks, int32_t* l, int32_t* parity, int32_t* sh_lmax,
+                                 int32_t* out_lmax, int32_t* flags) {
+    if (i < 0 || i >= kNumConfigs) return fail(E3GB_ERR_INVALID_ARG, "config index %d out of range", i);
+    const ConfigOps* o = kRegistry[i]();
+    const int nb = xcode_nblocks(o->xcode);
+    if (n_blocks) *n_blocks = nb;
+    for (int b = 0; b < nb; ++b) {
+        if (l) l[b] = xcode_l(o->xcode, b);
+        if (parity) parity[b] = xcode_p(o->xcode, b);
+    }
+    if (sh_lmax) *sh_lmax = o->L2;
+    if (out_lmax) *out_lmax = o->L3;
+    if (flags) *flags = o->per_path ? E3GB_PATHS_SEPARATE : E3GB_PATHS_SUMMED;
+    return ok();
+}
+
+e3gb_status e3gb_table_create(const e3gb_irreps* x, int32_t sh_lmax, int32_t out_lmax, int32_t flags,
+                              e3gb_table** out) {
+    if (out == nullptr) return fail(E3GB_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (x == nullptr || x->l == nullptr || x->parity == nullptr) return fail(E3GB_ERR_INVALID_ARG, "irreps is NULL");
+    if (x->n <= 0 || x->n > kMaxBlocks) return fail(E3GB_ERR_INVALID_ARG, "irreps: %d blocks (1..8)", x->n);
+    if (flags != E3GB_PATHS_SUMMED && flags != E3GB_PATHS_SEPARATE) return fail(E3GB_ERR_INVALID_ARG, "bad flags");
+    if (sh_lmax < 0 || sh_lmax > kLmax || out_lmax < 0 || out_lmax > kLmax)
+        return fail(E3GB_ERR_UNSUPPORTED, "sh_lmax and out_lmax must be in 0..3");
+    uint32_t code = 0;
+    for (int i = 0; i < x->n; ++i) {
+        if (x->l[i] < 0 || x->l[i] > kLmax) return fail(E3GB_ERR_UNSUPPORTED, "irreps block %d: l=%d not in 0..3", i, x->l[i]);
+        if (x->parity[i] != 1 && x->parity[i] != -1) return fail(E3GB_ERR_INVALID_ARG, "irreps block %d: parity must be +-1", i);
+        code |= xblock(x->l[i], x->parity[i]) << (4 * i);
+    }
+    if (!valid_mul(x->mul))
+        return fail(E3GB_ERR_UNSUPPORTED, "multiplicity %d: supported channel counts are 4, 8, 16, 32, 64, 128", x->mul);
+    for (int i = 0; i < kNumConfigs; ++i) {
+        const ConfigOps* o = kRegistry[i]();
+        if (o->xcode == code && o->L2 == sh_lmax && o->L3 == out_lmax && o->per_path == flags) {
+            *out = new e3gb_table{o, i, x->mul};
+            return ok();
+        }
+    }
+    return fail(E3GB_ERR_UNSUPPORTED, "irreps configuration has no compiled kernels (see e3gb_config_describe)");
+}
+
+e3gb_status e3gb_table_destroy(e3gb_table* t) {
+    delete t;
+    return ok();
+}
+
+e3gb_status e3gb_table_info(const e3gb_table* t, int32_t* d1, int32_t* d2, int32_t* n_paths, int32_t* D,
+                            int32_t* nnz, int32_t* mul) {
+    if (t == nullptr) return fail(E3GB_ERR_INVALID_ARG, "table is NULL");
+    if (d1) *d1 = t->ops->D1;
+    if (d2) *d2 = t->ops->D2;
+    if (n_paths) *n_paths = t->ops->NP;
+    if (D) *D = t->ops->D;
+    if (nnz) *nnz = t->ops->NR;
+    if (mul) *mul = t->mul;
+    return ok();
+}
+
+e3gb_status e3gb_table_paths(const e3gb_table* t, int32_t* paths) {
+    if (t == nullptr || paths == nullptr) return fail(E3GB_ERR_INVALID_ARG, "NULL argument");
+    for (int p = 0; p < t->ops->NP; ++p) {
+        const PathInfo& q = t->ops->paths[p];
+        const int32_t v[8] = {q.xblock, q.l1, q.p1, q.l2, q.l3, q.p3, q.out_block, q.zoff};
+        std::memcpy(paths + 8 * p, v, sizeof(v));
+    }
+    return ok();
+}
+
+e3gb_status e3gb_table_coefficients(const e3gb_table* t, double* rec) {
+    if (t == nullptr || rec == nullptr) return fail(E3GB_ERR_INVALID_ARG, "NULL argument");
+    for (int i = 0; i < t->ops->NR; ++i) {
+        const Rec& r = t->ops->recs[i];
+        rec[5 * i + 0] = r.path;
+        rec[5 * i + 1] = r.m1;
+        rec[5 * i + 2] = r.m2;
+        rec[5 * i + 3] = r.m3;
+        rec[5 * i + 4] = r.cd;
+    }
+    return ok();
+}
+
+e3gb_status e3gb_sh_forward(int32_t lmax, int64_t n, const float* vec, void* y, e3gb_dtype dtype, void* stream) {
+    if (lmax < 0 || lmax > kLmax) return fail(E3GB_ERR_UNSUPPORTED, "lmax %d not in 0..3", lmax);
+    if (n < 0) return fail(E3GB_ERR_INVALID_ARG, "n < 0");
+    if (dtype != E3GB_F32 && dtype != E3GB_BF16) return fail(E3GB_ERR_INVALID_ARG, "unknown dtype");
+    if (n == 0) return ok();
+    E3GB_TRY(check_ptr(vec, "vec", 4, true));
+    E3GB_TRY(check_ptr(y, "y", elt_bytes(dtype), true));
+    return cuda_status(sh_forward(lmax, n, vec, y, dtype == E3GB_BF16, (cudaStream_t)stream), "sh_forward launch");
+}
+
+e3gb_status e3gb_tp_forward(const e3gb_table* t, int64_t rows, const void* x, const void* y, const void* w, void* z,
+                            e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (rows < 0) return fail(E3GB_ERR_INVALID_ARG, "rows < 0");
+    if (rows == 0) return ok();
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, true));
+    E3GB_TRY(check_ptr(w, "w", va, true));
+    E3GB_TRY(check_ptr(z, "z", va, true));
+    return cuda_status(t->ops->tp_fwd[dtype](rows, t->mul, x, y, w, z, (cudaStream_t)stream), "tp_forward launch");
+}
+
+e3gb_status e3gb_tp_backward(const e3gb_table* t, int64_t rows, const void* x, const void* y, const void* w,
+                             const void* dz, void* dx, void* dy, void* dw, e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (rows < 0) return fail(E3GB_ERR_INVALID_ARG, "rows < 0");
+    if (rows == 0) return ok();
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, true));
+    E3GB_TRY(check_ptr(w, "w", va, true));
+    E3GB_TRY(check_ptr(dz, "dz", va, true));
+    E3GB_TRY(check_ptr(dx, "dx", va, true));
+    E3GB_TRY(check_ptr(dy, "dy", ea, true));
+    E3GB_TRY(check_ptr(dw, "dw", va, true));
+    return cuda_status(t->ops->tp_bwd[dtype](rows, t->mul, x, y, w, dz, dx, dy, dw, (cudaStream_t)stream),
+                       "tp_backward launch");
+}
+
+size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes) {
+    return n_nodes < 0 ? 0 : graph_workspace_bytes(n_nodes);
+}
+
+e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* rowptr, const int32_t* sender,
+                               int32_t* csc_ptr, int32_t* csc_edge, int32_t* csc_recv, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (n_nodes == 0 && n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+    if (ws_bytes < graph_workspace_bytes(n_nodes))
+        return fail(E3GB_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, graph_workspace_bytes(n_nodes));
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
+    E3GB_TRY(check_ptr(workspace, "workspace", 16, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, n_edges > 0));
+    E3GB_TRY(check_ptr(csc_edge, "csc_edge", 4, n_edges > 0));
+    E3GB_TRY(check_ptr(csc_recv, "csc_recv", 4, n_edges > 0));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, workspace, err,
+                                     (cudaStream_t)stream),
+                       "graph_prepare launch");
+}
+
+e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
+                              const int32_t* sender, const void* x, const void* y, const void* w, float scale,
+                              void* m, e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (n_nodes == 0) {
+        if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+        return ok();
+    }
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, edges));
+    E3GB_TRY(check_ptr(w, "w", va, edges));
+    E3GB_TRY(check_ptr(m, "m", va, true));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    return cuda_status(t->ops->conv_fwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m, err,
+                                               (cudaStream_t)stream),
+                       "conv_forward launch");
+}
+
+e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* csc_ptr,
+                               const int32_t* csc_edge, const int32_t* csc_recv, const void* x, const void* y,
+                               const void* w, const void* dm, float scale, void* dx, void* dy, void* dw,
+                               e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (n_nodes == 0) {
+        if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+        return ok();
+    }
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
+    E3GB_TRY(check_ptr(csc_edge, "csc_edge", 4, edges));
+    E3GB_TRY(check_ptr(csc_recv, "csc_recv", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, edges));
+    E3GB_TRY(check_ptr(w, "w", va, edges));
+    E3GB_TRY(check_ptr(dm, "dm", va, true));
+    E3GB_TRY(check_ptr(dx, "dx", va, true));
+    E3GB_TRY(check_ptr(dy, "dy", ea, edges));
+    E3GB_TRY(check_ptr(dw, "dw", va, edges));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    return cuda_status(t->ops->conv_bwd[dtype](n_nodes, n_edges, t->mul, csc_ptr, csc_edge, csc_recv, x, y, w, dm,
+                                               scale, dx, dy, dw, err, (cudaStream_t)stream),
+                       "conv_backward launch");
+}
+
+e3gb_status e3gb_check_device_status(void* stream, int32_t* flags) {
+    if (flags) *flags = 0;
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned host = 0;
+    E3GB_TRY(cuda_status(cudaMemcpyAsync(&host, err, sizeof(unsigned), cudaMemcpyDeviceToHost, s), "read error word"));
+    E3GB_TRY(cuda_status(cudaMemsetAsync(err, 0, sizeof(unsigned), s), "clear error word"));
+    E3GB_TRY(cuda_status(cudaStreamSynchronize(s), "cudaStreamSynchronize"));
+    if (flags) *flags = int32_t(host);
+    if (host != 0) return fail(E3GB_ERR_DEVICE_INDEX, "device saw out-of-range indices (flags 0x%x)", host);
+    return ok();
+}
+
+}  // extern "C"

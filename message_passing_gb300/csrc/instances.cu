@@ -1,0 +1,93 @@
+// One irreps configuration's kernels and launchers; compiled once per entry of configs.def
+// with -DE3GB_CFG=<id>, each unit exporting e3gb::ops_<id>().
+#include "kernels.cuh"
+
+#ifndef E3GB_CFG
+#error "compile with -DE3GB_CFG=<config id>"
+#endif
+
+namespace e3gb {
+
+template <class... B>
+constexpr uint32_t xcode(B... b) {
+    uint32_t c = 0;
+    int i = 0;
+    ((c |= uint32_t(b) << (4 * i++)), ...);
+    return c;
+}
+
+template <int ID>
+struct Pick;
+#define E3GB_CONFIG(ID, XC, L2, L3, PP) \
+    template <>                         \
+    struct Pick<ID> {                   \
+        using type = Config<XC, L2, L3, PP>; \
+    };
+#include "configs.def"
+#undef E3GB_CONFIG
+
+namespace {
+using Cfg = typename Pick<E3GB_CFG>::type;
+constexpr int kBlock = 256;
+
+int rows_per_block(int Nq) { return (kBlock / 32) * (32 / (Nq / kVec)); }
+
+template <class T>
+cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* w, void* z, cudaStream_t s) {
+    auto k = tp_forward_kernel<Cfg, T>;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (T*)z);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* w, const void* dz, void* dx,
+                   void* dy, void* dw, cudaStream_t s) {
+    auto k = tp_backward_kernel<Cfg, T>;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (const T*)dz, (T*)dx, (T*)dy,
+                              (T*)dw);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                     const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s) {
+    auto k = conv_forward_kernel<Cfg, T>;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (T*)m,
+                              err);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
+                     const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
+                     void* dw, unsigned* err, cudaStream_t s) {
+    auto k = conv_backward_kernel<Cfg, T>;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
+                              (const T*)dm, scale, (T*)dx, (T*)dy, (T*)dw, err);
+    return cudaGetLastError();
+}
+
+const ConfigOps kOps = {
+    Cfg::xcode, Cfg::L2, Cfg::L3, Cfg::per_path ? 1 : 0,
+    Cfg::NP, Cfg::D1, Cfg::D2, Cfg::D, Cfg::NOUT, Cfg::NR,
+    Cfg::table.paths.data(), Cfg::table.outs.data(), Cfg::recs.data(),
+    {tp_fwd<float>, tp_fwd<__nv_bfloat16>},
+    {tp_bwd<float>, tp_bwd<__nv_bfloat16>},
+    {conv_fwd<float>, conv_fwd<__nv_bfloat16>},
+    {conv_bwd<float>, conv_bwd<__nv_bfloat16>},
+};
+}  // namespace
+
+#define E3GB_CAT2(a, b) a##b
+#define E3GB_CAT(a, b) E3GB_CAT2(a, b)
+const ConfigOps* E3GB_CAT(ops_, E3GB_CFG)() { return &kOps; }
+
+}  // namespace e3gb

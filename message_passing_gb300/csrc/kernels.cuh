@@ -1,0 +1,518 @@
+// Tensor-product and convolution kernels, specialised at compile time per irreps
+// configuration (cg_table.hpp). Included by instances.cu once per configuration.
+//
+// Mapping ("e3j ...", App. E.2.1 "trailing channels"): lanes own channels, VEC = 4 adjacent
+// channels per lane (one 16-byte fp32 vector or one 8-byte bf16 vector), G = Nq/4 lanes per
+// row, 32/G rows per warp. Every lane walks the same unrolled sequence of CG couplings.
+//
+// Per row / edge, the SH operand y is contracted first with the CG block of each path:
+//   A_p[m3][m1] = sum_m2 C_p[m1][m2][m3] y[l2^2 + m2]        (lane-uniform, from immediates)
+// and then applied to every channel:
+//   z_p[m3][q] = sum_m1 A_p[m3][m1] x[l1 off + m1][q],  out[blk p][m3][q] += w[p][q] z_p[m3][q]
+// (the weight multiplies whichever side, x or z_p, is shorter). This is Eq. (13) with the
+// sum over i2 taken inside the per-edge uniform part, as Alg. 2 takes the sum over records
+// before applying the edge scalar.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <utility>
+
+#include "cg_table.hpp"
+
+namespace e3gb {
+
+constexpr int kVec = 4;
+
+// device error word bits
+constexpr unsigned kErrSender = 1u, kErrRowptr = 2u, kErrRecv = 4u;
+
+template <int... I, class F>
+__device__ __forceinline__ void sfor_impl(std::integer_sequence<int, I...>, F&& f) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+// static for: f(integral_constant<int, i>) for i = 0..N-1, fully unrolled
+template <int N, class F>
+__device__ __forceinline__ void sfor(F&& f) {
+    sfor_impl(std::make_integer_sequence<int, N>{}, f);
+}
+
+// ------------------------------------------------------------------------------------------
+// storage types
+// ------------------------------------------------------------------------------------------
+template <class T>
+struct IO;
+
+template <>
+struct IO<float> {
+    static __device__ __forceinline__ void load4(const float* __restrict__ p, float (&o)[4]) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(p));
+        o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    }
+    static __device__ __forceinline__ void store4(float* __restrict__ p, const float (&o)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    static __device__ __forceinline__ float load1(const float* __restrict__ p) { return __ldg(p); }
+    static __device__ __forceinline__ void store1(float* __restrict__ p, float v) { *p = v; }
+};
+
+template <>
+struct IO<__nv_bfloat16> {
+    static __device__ __forceinline__ void load4(const __nv_bfloat16* __restrict__ p, float (&o)[4]) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
+        const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+        o[0] = fa.x; o[1] = fa.y; o[2] = fb.x; o[3] = fb.y;
+    }
+    static __device__ __forceinline__ void store4(__nv_bfloat16* __restrict__ p, const float (&o)[4]) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(o[2], o[3]);
+        uint2 t;
+        t.x = *reinterpret_cast<const uint32_t*>(&a);
+        t.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(p) = t;
+    }
+    static __device__ __forceinline__ float load1(const __nv_bfloat16* __restrict__ p) {
+        return __bfloat162float(p[0]);
+    }
+    static __device__ __forceinline__ void store1(__nv_bfloat16* __restrict__ p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+// ------------------------------------------------------------------------------------------
+// per-configuration constant helpers
+// ------------------------------------------------------------------------------------------
+template <class Cfg>
+struct Off {
+    // offsets of each path's A-entries and CG records inside Cfg::aents / Cfg::recs
+    static constexpr std::array<int, Cfg::NP + 1> a = [] {
+        std::array<int, Cfg::NP + 1> o{};
+        for (int i = 0; i < Cfg::NA; ++i) o[Cfg::aents[i].path + 1]++;
+        for (int p = 0; p < Cfg::NP; ++p) o[p + 1] += o[p];
+        return o;
+    }();
+    static constexpr std::array<int, Cfg::NP + 1> r = [] {
+        std::array<int, Cfg::NP + 1> o{};
+        for (int i = 0; i < Cfg::NR; ++i) o[Cfg::recs[i].path + 1]++;
+        for (int p = 0; p < Cfg::NP; ++p) o[p + 1] += o[p];
+        return o;
+    }();
+    // first output offset of output block j
+    static constexpr std::array<int, Cfg::NOUT + 1> z = [] {
+        std::array<int, Cfg::NOUT + 1> o{};
+        for (int j = 0; j < Cfg::NOUT; ++j) o[j + 1] = o[j] + 2 * Cfg::table.outs[j].l + 1;
+        return o;
+    }();
+};
+
+// A_p entries for path P (compile-time), from the row's y values.
+template <class Cfg, int P>
+__device__ __forceinline__ void build_A(const float (&yv)[Cfg::D2], float (&A)[Off<Cfg>::a[P + 1] - Off<Cfg>::a[P]]) {
+    constexpr int a0 = Off<Cfg>::a[P];
+    constexpr int na = Off<Cfg>::a[P + 1] - a0;
+    constexpr int yo = Cfg::table.paths[P].yoff;
+    sfor<na>([&](auto k) {
+        constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+        float s = e.c[0] * yv[yo + e.m2[0]];
+        sfor<e.nt - 1>([&](auto t) {
+            constexpr int tt = decltype(t)::value + 1;
+            s = fmaf(e.c[tt], yv[yo + e.m2[tt]], s);
+        });
+        A[decltype(k)::value] = s;
+    });
+}
+
+// acc[m3][c] += w[c] * sum_m1 A[m3][m1] x[xoff + m1][c] for path P.
+template <class Cfg, int P, int NROWS>
+__device__ __forceinline__ void apply_path(const float (&A)[Off<Cfg>::a[P + 1] - Off<Cfg>::a[P]],
+                                           const float (&xv)[Cfg::D1][kVec], const float (&wv)[kVec],
+                                           float (&acc)[NROWS][kVec], int row0) {
+    constexpr PathInfo pi = Cfg::table.paths[P];
+    constexpr int a0 = Off<Cfg>::a[P];
+    constexpr int na = Off<Cfg>::a[P + 1] - a0;
+    constexpr int n1 = 2 * pi.l1 + 1, n3 = 2 * pi.l3 + 1;
+    if constexpr (n1 <= n3) {
+        float xw[n1][kVec];
+#pragma unroll
+        for (int m = 0; m < n1; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) xw[m][c] = wv[c] * xv[pi.xoff + m][c];
+        sfor<na>([&](auto k) {
+            constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+#pragma unroll
+            for (int c = 0; c < kVec; ++c)
+                acc[row0 + e.m3][c] = fmaf(A[decltype(k)::value], xw[e.m1][c], acc[row0 + e.m3][c]);
+        });
+    } else {
+        float t[n3][kVec];
+#pragma unroll
+        for (int m = 0; m < n3; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) t[m][c] = 0.f;
+        sfor<na>([&](auto k) {
+            constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+#pragma unroll
+            for (int c = 0; c < kVec; ++c)
+                t[e.m3][c] = fmaf(A[decltype(k)::value], xv[pi.xoff + e.m1][c], t[e.m3][c]);
+        });
+#pragma unroll
+        for (int m = 0; m < n3; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[row0 + m][c] = fmaf(wv[c], t[m][c], acc[row0 + m][c]);
+    }
+}
+
+struct Lanes {
+    int G;        // lanes per row
+    int grp;      // row slot inside the warp
+    int gl;       // lane inside the row group
+    int per_warp; // rows per warp
+};
+
+__device__ __forceinline__ Lanes lanes_for(int Nq) {
+    Lanes L;
+    L.G = Nq / kVec;
+    const int lane = threadIdx.x & 31;
+    L.grp = lane / L.G;
+    L.gl = lane % L.G;
+    L.per_warp = 32 / L.G;
+    return L;
+}
+
+// ------------------------------------------------------------------------------------------
+// TP forward on rows: output block by output block, so only one block's accumulators live.
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T>
+__global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, const T* __restrict__ x,
+                                                         const T* __restrict__ y, const T* __restrict__ w,
+                                                         T* __restrict__ z) {
+    const Lanes L = lanes_for(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * kVec;
+    for (int64_t r = warp * L.per_warp + L.grp; r < R; r += nwarp * L.per_warp) {
+        float yv[Cfg::D2];
+#pragma unroll
+        for (int i = 0; i < Cfg::D2; ++i) yv[i] = IO<T>::load1(y + r * Cfg::D2 + i);
+        float xv[Cfg::D1][kVec];
+#pragma unroll
+        for (int i = 0; i < Cfg::D1; ++i) IO<T>::load4(x + (r * Cfg::D1 + i) * Nq + c0, xv[i]);
+        sfor<Cfg::NOUT>([&](auto jj) {
+            constexpr int j = decltype(jj)::value;
+            constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
+            float acc[nrow][kVec];
+#pragma unroll
+            for (int m = 0; m < nrow; ++m)
+#pragma unroll
+                for (int c = 0; c < kVec; ++c) acc[m][c] = 0.f;
+            sfor<Cfg::NP>([&](auto pp) {
+                constexpr int p = decltype(pp)::value;
+                if constexpr (Cfg::table.paths[p].out_block == j) {
+                    float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
+                    build_A<Cfg, p>(yv, A);
+                    float wv[kVec];
+                    IO<T>::load4(w + (r * Cfg::NP + p) * Nq + c0, wv);
+                    apply_path<Cfg, p, nrow>(A, xv, wv, acc, 0);
+                }
+            });
+            constexpr int zo = Off<Cfg>::z[j];
+#pragma unroll
+            for (int m = 0; m < nrow; ++m) IO<T>::store4(z + (r * Cfg::D + zo + m) * Nq + c0, acc[m]);
+        });
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Backward body for one (row or edge) e: given x (of the row / sender), y[e], w[e] and the
+// cotangent rows g = scale * dz/dm (of the row / receiver), accumulate dx into dxa, the
+// lane's partial dy (summed over its channels) into dyp, and write dw[e].
+//   g_p[m1][q] = sum_m3 A_p[m3][m1] g[blk p][m3][q]
+//   dw[e,p,q]  = sum_m1 x[m1][q] g_p[m1][q]
+//   dx[m1][q] += w[p][q] g_p[m1][q]
+//   dy[m2]    += sum_{records (m1,m2,m3,c)} c * sum_q x[m1][q] w[p][q] g[m3][q]
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T>
+__device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], const float (&yv)[Cfg::D2],
+                                              const T* __restrict__ w_e, const T* __restrict__ g_row,
+                                              float gscale, T* __restrict__ dw_e, int Nq, int c0,
+                                              float (&dxa)[Cfg::D1][kVec], float (&dyp)[Cfg::D2]) {
+    sfor<Cfg::NOUT>([&](auto jj) {
+        constexpr int j = decltype(jj)::value;
+        constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
+        constexpr int zo = Off<Cfg>::z[j];
+        float g[nrow][kVec];
+#pragma unroll
+        for (int m = 0; m < nrow; ++m) {
+            IO<T>::load4(g_row + (zo + m) * Nq + c0, g[m]);
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) g[m][c] *= gscale;
+        }
+        sfor<Cfg::NP>([&](auto pp) {
+            constexpr int p = decltype(pp)::value;
+            constexpr PathInfo pi = Cfg::table.paths[p];
+            if constexpr (pi.out_block == j) {
+                constexpr int a0 = Off<Cfg>::a[p];
+                constexpr int na = Off<Cfg>::a[p + 1] - a0;
+                constexpr int n1 = 2 * pi.l1 + 1;
+                float A[na];
+                build_A<Cfg, p>(yv, A);
+                float wv[kVec];
+                IO<T>::load4(w_e + p * Nq + c0, wv);
+                float gp[n1][kVec];
+                float xw[n1][kVec];
+#pragma unroll
+                for (int m = 0; m < n1; ++m)
+#pragma unroll
+                    for (int c = 0; c < kVec; ++c) {
+                        gp[m][c] = 0.f;
+                        xw[m][c] = xv[pi.xoff + m][c] * wv[c];
+                    }
+                sfor<na>([&](auto k) {
+                    constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+                    float s = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kVec; ++c) {
+                        gp[e.m1][c] = fmaf(A[decltype(k)::value], g[e.m3][c], gp[e.m1][c]);
+                        s = fmaf(xw[e.m1][c], g[e.m3][c], s);
+                    }
+                    sfor<e.nt>([&](auto t) {
+                        constexpr int tt = decltype(t)::value;
+                        dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
+                    });
+                });
+                float dwv[kVec];
+#pragma unroll
+                for (int c = 0; c < kVec; ++c) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int m = 0; m < n1; ++m) {
+                        s = fmaf(xv[pi.xoff + m][c], gp[m][c], s);
+                        dxa[pi.xoff + m][c] = fmaf(wv[c], gp[m][c], dxa[pi.xoff + m][c]);
+                    }
+                    dwv[c] = s;
+                }
+                IO<T>::store4(dw_e + p * Nq + c0, dwv);
+            }
+        });
+    });
+}
+
+// Sum dyp over the G lanes of a row group (fixed butterfly order, deterministic).
+template <int N>
+__device__ __forceinline__ void group_reduce(float (&v)[N], int G) {
+    for (int off = G >> 1; off > 0; off >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], off);
+    }
+}
+
+template <class Cfg, class T>
+__global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, const T* __restrict__ x,
+                                                          const T* __restrict__ y, const T* __restrict__ w,
+                                                          const T* __restrict__ dz, T* __restrict__ dx,
+                                                          T* __restrict__ dy, T* __restrict__ dw) {
+    const Lanes L = lanes_for(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * kVec;
+    // every lane of the warp runs the same trip count so the group shuffles stay converged
+    const int64_t iters = (R + nwarp * L.per_warp - 1) / (nwarp * L.per_warp);
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t r = (it * nwarp + warp) * L.per_warp + L.grp;
+        const bool live = r < R;
+        const int64_t rr = live ? r : 0;
+        float yv[Cfg::D2], xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec], dyp[Cfg::D2];
+#pragma unroll
+        for (int i = 0; i < Cfg::D2; ++i) {
+            yv[i] = live ? IO<T>::load1(y + rr * Cfg::D2 + i) : 0.f;
+            dyp[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < Cfg::D1; ++i) {
+            if (live) IO<T>::load4(x + (rr * Cfg::D1 + i) * Nq + c0, xv[i]);
+            else
+#pragma unroll
+                for (int c = 0; c < kVec; ++c) xv[i][c] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) dxa[i][c] = 0.f;
+        }
+        if (live)
+            backward_body<Cfg, T>(xv, yv, w + rr * Cfg::NP * Nq, dz + rr * Cfg::D * Nq, 1.f,
+                                  dw + rr * Cfg::NP * Nq, Nq, c0, dxa, dyp);
+        group_reduce<Cfg::D2>(dyp, L.G);
+        if (live) {
+#pragma unroll
+            for (int i = 0; i < Cfg::D1; ++i) IO<T>::store4(dx + (rr * Cfg::D1 + i) * Nq + c0, dxa[i]);
+            if (L.gl == 0)
+#pragma unroll
+                for (int i = 0; i < Cfg::D2; ++i) IO<T>::store1(dy + rr * Cfg::D2 + i, dyp[i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Convolution forward: one row group per receiver, all D output rows in registers, edges
+// of the receiver in CSR order (Alg. 2 receiver-stationary aggregation).
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T>
+__global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E, int Nq,
+                                                           const int32_t* __restrict__ rowptr,
+                                                           const int32_t* __restrict__ sender,
+                                                           const T* __restrict__ x, const T* __restrict__ y,
+                                                           const T* __restrict__ w, float scale,
+                                                           T* __restrict__ m, unsigned* __restrict__ err) {
+    const Lanes L = lanes_for(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * kVec;
+    for (int64_t b = warp * L.per_warp + L.grp; b < N; b += nwarp * L.per_warp) {
+        float acc[Cfg::D][kVec];
+#pragma unroll
+        for (int i = 0; i < Cfg::D; ++i)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[i][c] = 0.f;
+        int64_t e0 = __ldg(rowptr + b), e1 = __ldg(rowptr + b + 1);
+        if (e0 < 0 || e1 < e0 || e1 > E) {
+            if (L.gl == 0) atomicOr(err, kErrRowptr);
+            e1 = e0 = 0;
+        }
+        for (int64_t e = e0; e < e1; ++e) {
+            const int64_t a = __ldg(sender + e);
+            if (a < 0 || a >= N) {
+                if (L.gl == 0) atomicOr(err, kErrSender);
+                continue;
+            }
+            float yv[Cfg::D2];
+#pragma unroll
+            for (int i = 0; i < Cfg::D2; ++i) yv[i] = IO<T>::load1(y + e * Cfg::D2 + i);
+            float xv[Cfg::D1][kVec];
+#pragma unroll
+            for (int i = 0; i < Cfg::D1; ++i) IO<T>::load4(x + (a * Cfg::D1 + i) * Nq + c0, xv[i]);
+            sfor<Cfg::NP>([&](auto pp) {
+                constexpr int p = decltype(pp)::value;
+                float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
+                build_A<Cfg, p>(yv, A);
+                float wv[kVec];
+                IO<T>::load4(w + (e * Cfg::NP + p) * Nq + c0, wv);
+                apply_path<Cfg, p, Cfg::D>(A, xv, wv, acc, Cfg::table.paths[p].zoff);
+            });
+        }
+#pragma unroll
+        for (int i = 0; i < Cfg::D; ++i) {
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[i][c] *= scale;
+            IO<T>::store4(m + (b * Cfg::D + i) * Nq + c0, acc[i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Convolution backward in sender order (the transposed graph of Eq. 16): one row group per
+// sender a; x[a] and the dx[a] accumulators stay in registers while the group walks the
+// edges of a (csc_ptr / csc_edge / csc_recv), gathering dm of each receiver. dw and dy are
+// edge-local and written once per edge.
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T>
+__global__ void __launch_bounds__(256) conv_backward_kernel(
+    int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
+    const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y,
+    const T* __restrict__ w, const T* __restrict__ dm, float scale, T* __restrict__ dx, T* __restrict__ dy,
+    T* __restrict__ dw, unsigned* __restrict__ err) {
+    const Lanes L = lanes_for(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * kVec;
+    const int64_t iters = (N + nwarp * L.per_warp - 1) / (nwarp * L.per_warp);
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t a = (it * nwarp + warp) * L.per_warp + L.grp;
+        const bool live = a < N;
+        const int64_t aa = live ? a : 0;
+        float xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec];
+#pragma unroll
+        for (int i = 0; i < Cfg::D1; ++i) {
+            if (live) IO<T>::load4(x + (aa * Cfg::D1 + i) * Nq + c0, xv[i]);
+            else
+#pragma unroll
+                for (int c = 0; c < kVec; ++c) xv[i][c] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) dxa[i][c] = 0.f;
+        }
+        int64_t k0 = 0, k1 = 0;
+        if (live) {
+            k0 = __ldg(csc_ptr + aa);
+            k1 = __ldg(csc_ptr + aa + 1);
+            if (k0 < 0 || k1 < k0 || k1 > E) {
+                if (L.gl == 0) atomicOr(err, kErrRowptr);
+                k0 = k1 = 0;
+            }
+        }
+        // the row groups of a warp may own different edge counts; loop to the warp maximum
+        int64_t cnt = k1 - k0, wmax = cnt;
+        for (int off = 16; off > 0; off >>= 1) {
+            const int64_t o = __shfl_xor_sync(0xffffffffu, wmax, off);
+            wmax = o > wmax ? o : wmax;
+        }
+        for (int64_t i = 0; i < wmax; ++i) {
+            bool ok = i < cnt;
+            int64_t e = 0, b = 0;
+            if (ok) {
+                e = __ldg(csc_edge + k0 + i);
+                b = __ldg(csc_recv + k0 + i);
+                if (e < 0 || e >= E || b < 0 || b >= N) {
+                    if (L.gl == 0) atomicOr(err, kErrRecv);
+                    ok = false;
+                }
+            }
+            float dyp[Cfg::D2];
+#pragma unroll
+            for (int t = 0; t < Cfg::D2; ++t) dyp[t] = 0.f;
+            if (ok) {
+                float yv[Cfg::D2];
+#pragma unroll
+                for (int t = 0; t < Cfg::D2; ++t) yv[t] = IO<T>::load1(y + e * Cfg::D2 + t);
+                backward_body<Cfg, T>(xv, yv, w + e * Cfg::NP * Nq, dm + b * Cfg::D * Nq, scale,
+                                      dw + e * Cfg::NP * Nq, Nq, c0, dxa, dyp);
+            }
+            group_reduce<Cfg::D2>(dyp, L.G);
+            if (ok && L.gl == 0)
+#pragma unroll
+                for (int t = 0; t < Cfg::D2; ++t) IO<T>::store1(dy + e * Cfg::D2 + t, dyp[t]);
+        }
+        if (live)
+#pragma unroll
+            for (int i = 0; i < Cfg::D1; ++i) IO<T>::store4(dx + (aa * Cfg::D1 + i) * Nq + c0, dxa[i]);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// host-side launch table of one configuration
+// ------------------------------------------------------------------------------------------
+struct Launch {
+    int grid, block;
+};
+
+struct ConfigOps {
+    uint32_t xcode;
+    int L2, L3, per_path;
+    int NP, D1, D2, D, NOUT, NR;
+    const PathInfo* paths;
+    const OutBlock* outs;
+    const Rec* recs;
+    // kernels (dtype 0 = fp32, 1 = bf16); each returns cudaError_t of the launch
+    cudaError_t (*tp_fwd[2])(int64_t, int, const void*, const void*, const void*, void*, cudaStream_t);
+    cudaError_t (*tp_bwd[2])(int64_t, int, const void*, const void*, const void*, const void*, void*, void*,
+                             void*, cudaStream_t);
+    cudaError_t (*conv_fwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
+                               const void*, const void*, float, void*, unsigned*, cudaStream_t);
+    cudaError_t (*conv_bwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                               const void*, const void*, const void*, const void*, float, void*, void*,
+                               void*, unsigned*, cudaStream_t);
+};
+
+int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units);
+
+}  // namespace e3gb

@@ -229,3 +229,21 @@ def random_graph(n_nodes: int, n_edges: int, key: tuple[int, ...], empty_nodes: 
     np.cumsum(np.bincount(recv, minlength=n_nodes), out=rowptr[1:])
     vec = g.standard_normal((n_edges, 3))
     return Graph(n_nodes, rowptr.astype(np.int32), send.astype(np.int32), vec, 0.0, 0.0, "random")
+
+
+def device_normal(shape: tuple[int, ...], key: tuple[int, ...], scale: float = 1.0, device="cuda",
+                  dtype=None):
+    """Seeded N(0, scale^2) float32 tensor drawn on the GPU with torch's generator (for inputs
+    of tens of GB, e.g. the per-edge weights of the 64k-atom workload). The seed is derived
+    from key like the host streams; both sides of a comparison read the same tensor (the
+    oracle copies the rows it samples to the host)."""
+    import torch
+    seed = int(np.random.SeedSequence([int(k) for k in key]).generate_state(1, np.uint64)[0] >> np.uint64(1))
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if scale != 1.0:
+        t.mul_(scale)
+    if dtype is not None and dtype != torch.float32:
+        t = t.to(dtype)
+    return t

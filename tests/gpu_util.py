@@ -1,0 +1,45 @@
+"""Helpers shared by the GPU parity tests (no method arithmetic here)."""
+from __future__ import annotations
+
+import numpy as np
+
+# fp32 I/O: max |err| <= 1e-5 RMS(ref); bf16 storage: <= 2e-2 RMS(ref) (per output tensor)
+TOL_F32 = 1e-5
+TOL_BF16 = 2e-2
+
+
+def assert_close(got, ref, tol: float, name: str = ""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    bound = tol * rms if rms > 0 else 1e-30
+    assert err <= bound, f"{name}: max|err| {err:.3e} > {tol:g} x RMS {rms:.3e} (ratio {err / max(rms, 1e-300):.2e})"
+    return err / rms if rms > 0 else 0.0
+
+
+def to_dev(a, dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if dtype is not None:
+        t = t.to(dtype)
+    return t
+
+
+def to_np(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def sample_ids(n: int, k: int, seed: int) -> np.ndarray:
+    """k distinct indices in [0, n): the first three, the last three and random ones, sorted."""
+    if n <= k:
+        return np.arange(n)
+    rng = np.random.default_rng(seed)
+    ids = set([0, 1, 2, n - 3, n - 2, n - 1])
+    ids.update(rng.choice(n, size=k - len(ids), replace=False).tolist())
+    return np.array(sorted(ids)[:k], dtype=np.int64)
