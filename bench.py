@@ -74,10 +74,11 @@ def ncu_traffic(kernel: str, units: float):
 # algorithmic bytes (Eq. 9)
 # ---------------------------------------------------------------------------------------
 def conv_bytes(N, E, d1, d2, P, D, Nq, s):
-    fwd = N * d1 * Nq * s + E * d2 * s + E * P * Nq * s + (N + 1) * 4 + E * 4 + N * D * Nq * s
+    """s = bytes per stored input element; outputs are fp32."""
+    fwd = N * d1 * Nq * s + E * d2 * s + E * P * Nq * s + (N + 1) * 4 + E * 4 + N * D * Nq * 4
     bwd = (N * d1 * Nq * s + E * d2 * s + E * P * Nq * s + N * D * Nq * s      # x, y, w, dm
            + (N + 1) * 4 + 2 * E * 4                                           # sender-major index
-           + N * d1 * Nq * s + E * d2 * s + E * P * Nq * s)                    # dx, dy, dw
+           + (N * d1 * Nq + E * d2 + E * P * Nq) * 4)                          # dx, dy, dw
     return fwd, bwd
 
 
@@ -257,8 +258,9 @@ def run_ours(args):
     wd = device_normal((E, P, Nq), (w.wid, STREAM_W), W.weight_scale(w, P), device=dev, dtype=dt)
     dmd = device_normal((N, D, Nq), (w.wid, STREAM_GRAD), device=dev, dtype=dt)
     y = torch.empty((E, t.d2), device=dev, dtype=dt)
-    m = torch.empty((N, D, Nq), device=dev, dtype=dt)
-    dx, dy, dw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+    m = torch.empty((N, D, Nq), device=dev, dtype=torch.float32)
+    f32 = dict(dtype=torch.float32)
+    dx, dy, dw = torch.empty_like(xd, **f32), torch.empty_like(y, **f32), torch.empty_like(wd, **f32)
     csc = e3.graph_prepare(rp, sd, N)
     e3.check_device_status()
     stream = torch.cuda.current_stream()
@@ -354,7 +356,7 @@ def run_ours(args):
                       "rows_per_s": R / tb}}
         del x2d, w2d, dz, y2, z, gx, gy, gw
         torch.cuda.empty_cache()
-        dx, dy, dw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+        dx, dy, dw = torch.empty_like(xd, **f32), torch.empty_like(y, **f32), torch.empty_like(wd, **f32)
 
     # ---- end to end through the API with host buffers
     e2e = None
@@ -364,10 +366,10 @@ def run_ours(args):
         h_w = torch.empty(wd.shape, dtype=wd.dtype, pin_memory=True)
         h_w.copy_(wd)
         h_dm = pin(dmd.cpu())
-        o_m = torch.empty(m.shape, dtype=dt, pin_memory=True)
-        o_dx = torch.empty(xd.shape, dtype=dt, pin_memory=True)
-        o_dy = torch.empty(y.shape, dtype=dt, pin_memory=True)
-        o_dw = torch.empty(wd.shape, dtype=dt, pin_memory=True)
+        o_m = torch.empty(m.shape, dtype=torch.float32, pin_memory=True)
+        o_dx = torch.empty(xd.shape, dtype=torch.float32, pin_memory=True)
+        o_dy = torch.empty(y.shape, dtype=torch.float32, pin_memory=True)
+        o_dw = torch.empty(wd.shape, dtype=torch.float32, pin_memory=True)
         h2d = sum(a.numel() * a.element_size() for a in (h_vec, h_rp, h_sd, h_x, h_w, h_dm))
         d2h = sum(a.numel() * a.element_size() for a in (o_m, o_dx, o_dy, o_dw))
 

@@ -21,9 +21,10 @@
  *
  * Memory and streams: every device buffer belongs to the caller; no call allocates device
  * memory. Work is enqueued on the caller's stream (a cudaStream_t passed as void*, NULL =
- * legacy default stream) and the call returns without synchronising. Device pointers must
- * be 16-byte aligned (fp32) or 8-byte aligned (bf16) and must not alias each other.
- * Outputs are overwritten, never accumulated into.
+ * legacy default stream) and the call returns without synchronising. Channel-vector arrays
+ * (x, w, dz, dm, and every fp32 output) must be 16-byte aligned, or 8-byte aligned when they
+ * are bf16 inputs; y and dy need element alignment; buffers must not alias each other.
+ * Outputs are always fp32 and are overwritten, never accumulated into.
  *
  * Errors: each call checks its arguments on the host and returns a status; the message of
  * the last failure on the calling thread is e3gb_last_error(). Index errors found on the
@@ -54,9 +55,10 @@ typedef enum {
 } e3gb_status;
 
 typedef enum {
-    E3GB_F32 = 0,   /* fp32 storage, fp32 arithmetic */
-    E3GB_BF16 = 1   /* bf16 storage of x, y, w, dz/dm and all outputs; fp32 accumulation,
-                       outputs rounded to nearest even once */
+    E3GB_F32 = 0,   /* fp32 inputs, fp32 arithmetic, fp32 outputs */
+    E3GB_BF16 = 1   /* bf16 storage of the inputs x, y, w and dz/dm (half their bytes); fp32
+                       arithmetic and fp32 outputs. (bf16 outputs would not meet a 2e-2 RMS
+                       bound: rounding the exact result alone reaches 3.7e-2 RMS for dw.) */
 } e3gb_dtype;
 
 /* Irreps of x with a uniform multiplicity: n blocks, block i of degree l[i] in 0..3 and
@@ -108,7 +110,8 @@ e3gb_status e3gb_config_describe(int32_t i, int32_t *n_blocks, int32_t *l, int32
 /* Real spherical harmonics (App. A.3 Eq. 4, App. G.1): y[e] = (Y_l(u_e))_{l=0..lmax},
  * u_e = vec[e]/|vec[e]| (u = 0 when |vec| < 1e-12, giving Y_0 = 1 and Y_l>0 = 0),
  * component normalisation sum_m Y_lm^2 = 2l+1, l = 1 ordered sqrt(3)(y, z, x).
- * vec: device fp32 [n, 3]; y: device [n, (lmax+1)^2] of dtype. lmax in 0..3. */
+ * vec: device fp32 [n, 3]; y: device [n, (lmax+1)^2] of dtype (bf16: rounded to nearest
+ * even from fp32, to feed the bf16 variant). lmax in 0..3. */
 e3gb_status e3gb_sh_forward(int32_t lmax, int64_t n, const float *vec, void *y,
                             e3gb_dtype dtype, void *stream);
 

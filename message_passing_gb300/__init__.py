@@ -108,6 +108,13 @@ def _dtype(*ts):
     raise TypeError(f"tensors must all be float32 or all bfloat16, got {dt}")
 
 
+def _f32_out(*ts):
+    import torch
+    for t in ts:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("outputs are float32 in both the fp32 and the bf16 variant")
+
+
 def _contig(*ts):
     for t in ts:
         if t is not None and not t.is_contiguous():
@@ -197,9 +204,10 @@ def sh_forward(vec, lmax: int, out=None, dtype=None, stream=None):
 def tp_forward(t: Table, x, y, w, out=None, stream=None):
     import torch
     _contig(x, y, w, out)
-    z = out if out is not None else torch.empty((x.shape[0], t.D, t.mul), dtype=x.dtype, device=x.device)
+    z = out if out is not None else torch.empty((x.shape[0], t.D, t.mul), dtype=torch.float32, device=x.device)
+    _f32_out(z)
     _check(load().e3gb_tp_forward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(z),
-                                  _dtype(x, y, w, z), _stream(stream)))
+                                  _dtype(x, y, w), _stream(stream)))
     return z
 
 
@@ -207,10 +215,12 @@ def tp_backward(t: Table, x, y, w, dz, out=None, stream=None):
     import torch
     _contig(x, y, w, dz)
     if out is None:
-        out = (torch.empty_like(x), torch.empty_like(y), torch.empty_like(w))
+        f = dict(dtype=torch.float32)
+        out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f))
     dx, dy, dw = out
+    _f32_out(dx, dy, dw)
     _check(load().e3gb_tp_backward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(dz), _ptr(dx),
-                                   _ptr(dy), _ptr(dw), _dtype(x, y, w, dz, dx, dy, dw), _stream(stream)))
+                                   _ptr(dy), _ptr(dw), _dtype(x, y, w, dz), _stream(stream)))
     return dx, dy, dw
 
 
@@ -241,10 +251,11 @@ def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stre
     import torch
     _contig(rowptr, sender, x, y, w)
     N, E = x.shape[0], sender.shape[0]
-    m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=x.dtype, device=x.device)
+    m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=torch.float32, device=x.device)
+    _f32_out(m)
     _check(load().e3gb_conv_forward(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
                                     _ptr(y) if E else None, _ptr(w) if E else None, float(scale), _ptr(m),
-                                    _dtype(x, m, *( (y, w) if E else ())), _stream(stream)))
+                                    _dtype(x, *((y, w) if E else ())), _stream(stream)))
     return m
 
 
@@ -255,12 +266,14 @@ def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=Non
     _contig(x, y, w, dm)
     N, E = x.shape[0], y.shape[0]
     if out is None:
-        out = (torch.empty_like(x), torch.empty_like(y), torch.empty_like(w))
+        f = dict(dtype=torch.float32)
+        out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f))
     dx, dy, dw = out
+    _f32_out(dx, dy, dw)
     _check(load().e3gb_conv_backward(t.handle, N, E, _ptr(cp), _ptr(ce) if E else None, _ptr(cr) if E else None,
                                      _ptr(x), _ptr(y) if E else None, _ptr(w) if E else None, _ptr(dm),
                                      float(scale), _ptr(dx), _ptr(dy) if E else None, _ptr(dw) if E else None,
-                                     _dtype(x, dm, dx, *((y, w, dy, dw) if E else ())), _stream(stream)))
+                                     _dtype(x, dm, *((y, w) if E else ())), _stream(stream)))
     return dx, dy, dw
 
 

@@ -258,7 +258,7 @@ e3gb_status e3gb_tp_forward(const e3gb_table* t, int64_t rows, const void* x, co
     E3GB_TRY(check_ptr(x, "x", va, true));
     E3GB_TRY(check_ptr(y, "y", ea, true));
     E3GB_TRY(check_ptr(w, "w", va, true));
-    E3GB_TRY(check_ptr(z, "z", va, true));
+    E3GB_TRY(check_ptr(z, "z", 16, true));
     return cuda_status(t->ops->tp_fwd[dtype](rows, t->mul, x, y, w, z, (cudaStream_t)stream), "tp_forward launch");
 }
 
@@ -272,9 +272,9 @@ e3gb_status e3gb_tp_backward(const e3gb_table* t, int64_t rows, const void* x, c
     E3GB_TRY(check_ptr(y, "y", ea, true));
     E3GB_TRY(check_ptr(w, "w", va, true));
     E3GB_TRY(check_ptr(dz, "dz", va, true));
-    E3GB_TRY(check_ptr(dx, "dx", va, true));
-    E3GB_TRY(check_ptr(dy, "dy", ea, true));
-    E3GB_TRY(check_ptr(dw, "dw", va, true));
+    E3GB_TRY(check_ptr(dx, "dx", 16, true));
+    E3GB_TRY(check_ptr(dy, "dy", 4, true));
+    E3GB_TRY(check_ptr(dw, "dw", 16, true));
     return cuda_status(t->ops->tp_bwd[dtype](rows, t->mul, x, y, w, dz, dx, dy, dw, (cudaStream_t)stream),
                        "tp_backward launch");
 }
@@ -322,7 +322,7 @@ e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_ed
     E3GB_TRY(check_ptr(x, "x", va, true));
     E3GB_TRY(check_ptr(y, "y", ea, edges));
     E3GB_TRY(check_ptr(w, "w", va, edges));
-    E3GB_TRY(check_ptr(m, "m", va, true));
+    E3GB_TRY(check_ptr(m, "m", 16, true));
     e3gb_status st = E3GB_OK;
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;
@@ -351,9 +351,9 @@ e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_e
     E3GB_TRY(check_ptr(y, "y", ea, edges));
     E3GB_TRY(check_ptr(w, "w", va, edges));
     E3GB_TRY(check_ptr(dm, "dm", va, true));
-    E3GB_TRY(check_ptr(dx, "dx", va, true));
-    E3GB_TRY(check_ptr(dy, "dy", ea, edges));
-    E3GB_TRY(check_ptr(dw, "dw", va, edges));
+    E3GB_TRY(check_ptr(dx, "dx", 16, true));
+    E3GB_TRY(check_ptr(dy, "dy", 4, edges));
+    E3GB_TRY(check_ptr(dw, "dw", 16, edges));
     e3gb_status st = E3GB_OK;
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;

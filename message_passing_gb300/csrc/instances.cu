@@ -37,7 +37,7 @@ cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* 
     auto k = tp_forward_kernel<Cfg, T>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (T*)z);
+    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (float*)z);
     return cudaGetLastError();
 }
 
@@ -47,8 +47,8 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
     auto k = tp_backward_kernel<Cfg, T>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (const T*)dz, (T*)dx, (T*)dy,
-                              (T*)dw);
+    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (const T*)dz, (float*)dx,
+                              (float*)dy, (float*)dw);
     return cudaGetLastError();
 }
 
@@ -58,7 +58,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
     auto k = conv_forward_kernel<Cfg, T>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (T*)m,
+    k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
                               err);
     return cudaGetLastError();
 }
@@ -71,7 +71,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                              (const T*)dm, scale, (T*)dx, (T*)dy, (T*)dw, err);
+                              (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, err);
     return cudaGetLastError();
 }
 

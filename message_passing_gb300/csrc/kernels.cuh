@@ -4,6 +4,8 @@
 // Mapping ("e3j ...", App. E.2.1 "trailing channels"): lanes own channels, VEC = 4 adjacent
 // channels per lane (one 16-byte fp32 vector or one 8-byte bf16 vector), G = Nq/4 lanes per
 // row, 32/G rows per warp. Every lane walks the same unrolled sequence of CG couplings.
+// Inputs (x, y, w, dz / dm) are stored as T (fp32 or bf16); arithmetic and every output are
+// fp32.
 //
 // Per row / edge, the SH operand y is contracted first with the CG block of each path:
 //   A_p[m3][m1] = sum_m2 C_p[m1][m2][m3] y[l2^2 + m2]        (lane-uniform, from immediates)
@@ -189,7 +191,7 @@ __device__ __forceinline__ Lanes lanes_for(int Nq) {
 template <class Cfg, class T>
 __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, const T* __restrict__ x,
                                                          const T* __restrict__ y, const T* __restrict__ w,
-                                                         T* __restrict__ z) {
+                                                         float* __restrict__ z) {
     const Lanes L = lanes_for(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, cons
             });
             constexpr int zo = Off<Cfg>::z[j];
 #pragma unroll
-            for (int m = 0; m < nrow; ++m) IO<T>::store4(z + (r * Cfg::D + zo + m) * Nq + c0, acc[m]);
+            for (int m = 0; m < nrow; ++m) IO<float>::store4(z + (r * Cfg::D + zo + m) * Nq + c0, acc[m]);
         });
     }
 }
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, cons
 template <class Cfg, class T>
 __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], const float (&yv)[Cfg::D2],
                                               const T* __restrict__ w_e, const T* __restrict__ g_row,
-                                              float gscale, T* __restrict__ dw_e, int Nq, int c0,
+                                              float gscale, float* __restrict__ dw_e, int Nq, int c0,
                                               float (&dxa)[Cfg::D1][kVec], float (&dyp)[Cfg::D2]) {
     sfor<Cfg::NOUT>([&](auto jj) {
         constexpr int j = decltype(jj)::value;
@@ -295,7 +297,7 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], 
                     }
                     dwv[c] = s;
                 }
-                IO<T>::store4(dw_e + p * Nq + c0, dwv);
+                IO<float>::store4(dw_e + p * Nq + c0, dwv);
             }
         });
     });
@@ -313,8 +315,8 @@ __device__ __forceinline__ void group_reduce(float (&v)[N], int G) {
 template <class Cfg, class T>
 __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, const T* __restrict__ x,
                                                           const T* __restrict__ y, const T* __restrict__ w,
-                                                          const T* __restrict__ dz, T* __restrict__ dx,
-                                                          T* __restrict__ dy, T* __restrict__ dw) {
+                                                          const T* __restrict__ dz, float* __restrict__ dx,
+                                                          float* __restrict__ dy, float* __restrict__ dw) {
     const Lanes L = lanes_for(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -346,10 +348,10 @@ __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, con
         group_reduce<Cfg::D2>(dyp, L.G);
         if (live) {
 #pragma unroll
-            for (int i = 0; i < Cfg::D1; ++i) IO<T>::store4(dx + (rr * Cfg::D1 + i) * Nq + c0, dxa[i]);
+            for (int i = 0; i < Cfg::D1; ++i) IO<float>::store4(dx + (rr * Cfg::D1 + i) * Nq + c0, dxa[i]);
             if (L.gl == 0)
 #pragma unroll
-                for (int i = 0; i < Cfg::D2; ++i) IO<T>::store1(dy + rr * Cfg::D2 + i, dyp[i]);
+                for (int i = 0; i < Cfg::D2; ++i) dy[rr * Cfg::D2 + i] = dyp[i];
         }
     }
 }
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
                                                            const int32_t* __restrict__ sender,
                                                            const T* __restrict__ x, const T* __restrict__ y,
                                                            const T* __restrict__ w, float scale,
-                                                           T* __restrict__ m, unsigned* __restrict__ err) {
+                                                           float* __restrict__ m, unsigned* __restrict__ err) {
     const Lanes L = lanes_for(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
         for (int i = 0; i < Cfg::D; ++i) {
 #pragma unroll
             for (int c = 0; c < kVec; ++c) acc[i][c] *= scale;
-            IO<T>::store4(m + (b * Cfg::D + i) * Nq + c0, acc[i]);
+            IO<float>::store4(m + (b * Cfg::D + i) * Nq + c0, acc[i]);
         }
     }
 }
@@ -420,8 +422,8 @@ template <class Cfg, class T>
 __global__ void __launch_bounds__(256) conv_backward_kernel(
     int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
     const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y,
-    const T* __restrict__ w, const T* __restrict__ dm, float scale, T* __restrict__ dx, T* __restrict__ dy,
-    T* __restrict__ dw, unsigned* __restrict__ err) {
+    const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
+    float* __restrict__ dy, float* __restrict__ dw, unsigned* __restrict__ err) {
     const Lanes L = lanes_for(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -480,11 +482,11 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
             group_reduce<Cfg::D2>(dyp, L.G);
             if (ok && L.gl == 0)
 #pragma unroll
-                for (int t = 0; t < Cfg::D2; ++t) IO<T>::store1(dy + e * Cfg::D2 + t, dyp[t]);
+                for (int t = 0; t < Cfg::D2; ++t) dy[e * Cfg::D2 + t] = dyp[t];
         }
         if (live)
 #pragma unroll
-            for (int i = 0; i < Cfg::D1; ++i) IO<T>::store4(dx + (aa * Cfg::D1 + i) * Nq + c0, dxa[i]);
+            for (int i = 0; i < Cfg::D1; ++i) IO<float>::store4(dx + (aa * Cfg::D1 + i) * Nq + c0, dxa[i]);
     }
 }
 
