@@ -144,6 +144,26 @@ e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t *
                                int32_t *csc_recv, void *workspace, size_t ws_bytes,
                                void *stream);
 
+/* Largest n_nodes that e3gb_graph_prepare_static accepts. */
+#define E3GB_STATIC_PREPARE_MAX_NODES 1048575
+
+/* e3gb_graph_prepare for callers that cannot allocate device memory. The paper has no
+ * counterpart: this entry point exists for programs that must not call cudaMalloc after
+ * start-up, for example a host that has handed all free device memory to its own pool, a
+ * plugin inside a host that owns every allocation and offers it no allocator, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation. It computes exactly what e3gb_graph_prepare computes, but keeps the
+ * per-node counters in a 4 MiB array inside the library (one per device that loads the
+ * library, held until the process exits) instead of a caller workspace; it allocates
+ * nothing. Limit: n_nodes <= E3GB_STATIC_PREPARE_MAX_NODES, else E3GB_ERR_INVALID_ARG.
+ * The first call on a device looks up the array's device address on that device; make that
+ * first call before any stream capture. All calls share the one array, and the call clears
+ * it on the stream before use: calls that overlap on the GPU (on different streams, or from
+ * different threads) race on it and must be serialised by the caller. */
+e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const int32_t *rowptr,
+                                      const int32_t *sender, int32_t *csc_ptr, int32_t *csc_edge,
+                                      int32_t *csc_recv, void *stream);
+
 /* Message-passing convolution (Eq. 12-13): for every receiver b,
  *   m[b] = scale * sum_{e in [rowptr[b], rowptr[b+1])} TP(x[sender[e]], y[e], w[e]),
  * accumulated in a fixed order in registers, written once (receivers without edges get 0).

@@ -26,7 +26,7 @@ SYMBOLS = (
     "e3gb_table_create", "e3gb_table_destroy", "e3gb_table_info", "e3gb_table_paths",
     "e3gb_table_coefficients", "e3gb_config_count", "e3gb_config_describe", "e3gb_sh_forward",
     "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
-    "e3gb_graph_prepare", "e3gb_conv_forward", "e3gb_conv_backward",
+    "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
 )
 
@@ -69,6 +69,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_tp_backward": (i32, [vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp]),
         "e3gb_graph_prepare_workspace_bytes": (szt, [i64]),
         "e3gb_graph_prepare": (i32, [i64, i64, vp, vp, vp, vp, vp, vp, szt, vp]),
+        "e3gb_graph_prepare_static": (i32, [i64, i64, vp, vp, vp, vp, vp, vp]),
         "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, vp, i32, vp]),
         "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, i32, vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
@@ -244,6 +245,28 @@ def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream
     _check(load().e3gb_graph_prepare(n_nodes, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(cp),
                                      _ptr(ce) if E else None, _ptr(cr) if E else None, _ptr(ws),
                                      ws.numel() * ws.element_size(), _stream(stream)))
+    return cp, ce, cr
+
+
+STATIC_PREPARE_MAX_NODES = 1048575
+
+
+def graph_prepare_static(rowptr, sender, n_nodes: int, out=None, stream=None):
+    """graph_prepare without a workspace, for callers that cannot allocate device memory:
+    the library keeps the counters in its own static device array (at most
+    STATIC_PREPARE_MAX_NODES nodes; calls overlapping on the GPU race on it). Pass ``out``
+    to avoid allocating the outputs here too."""
+    import torch
+    _contig(rowptr, sender)
+    E = sender.shape[0]
+    dev = rowptr.device
+    if out is None:
+        out = (torch.empty(n_nodes + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(E, 1), dtype=torch.int32, device=dev),
+               torch.empty(max(E, 1), dtype=torch.int32, device=dev))
+    cp, ce, cr = out
+    _check(load().e3gb_graph_prepare_static(n_nodes, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(cp),
+                                            _ptr(ce) if E else None, _ptr(cr) if E else None, _stream(stream)))
     return cp, ce, cr
 
 

@@ -305,6 +305,60 @@ e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* 
                        "graph_prepare launch");
 }
 
+// Allocation-free variant of e3gb_graph_prepare (see the header for who needs it): the
+// per-node counters live in this file-scope array. Host code must not pass the symbol
+// itself to a kernel (in host code it names a host-side stand-in); the device address is
+// looked up once per device with cudaGetSymbolAddress and passed on.
+static __device__ __align__(256) int32_t e3gb_prepare_scratch[E3GB_STATIC_PREPARE_MAX_NODES + 1];
+
+static int32_t* prepare_scratch(e3gb_status* st) {
+    static std::mutex mu;
+    static std::unordered_map<int, int32_t*> addr;   // device -> address of the array there
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_status(e, "cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, e3gb_prepare_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        *st = cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "cudaGetSymbolAddress(prepare scratch)");
+        return nullptr;
+    }
+    addr.emplace(dev, static_cast<int32_t*>(p));
+    return static_cast<int32_t*>(p);
+}
+
+e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const int32_t* rowptr, const int32_t* sender,
+                                      int32_t* csc_ptr, int32_t* csc_edge, int32_t* csc_recv, void* stream) {
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes > E3GB_STATIC_PREPARE_MAX_NODES)
+        return fail(E3GB_ERR_INVALID_ARG,
+                    "n_nodes %lld exceeds the static scratch of e3gb_graph_prepare_static (at most %d nodes); "
+                    "use e3gb_graph_prepare with a workspace",
+                    (long long)n_nodes, E3GB_STATIC_PREPARE_MAX_NODES);
+    if (n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "n_edges must be < 2^31-1");
+    if (n_nodes == 0 && n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, n_edges > 0));
+    E3GB_TRY(check_ptr(csc_edge, "csc_edge", 4, n_edges > 0));
+    E3GB_TRY(check_ptr(csc_recv, "csc_recv", 4, n_edges > 0));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    int32_t* scratch = prepare_scratch(&st);
+    if (scratch == nullptr) return st;
+    // the shared graph_prepare path zeroes the counters on the stream before using them
+    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, scratch, err,
+                                     (cudaStream_t)stream),
+                       "graph_prepare_static launch");
+}
+
 e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
                               const int32_t* sender, const void* x, const void* y, const void* w, float scale,
                               void* m, e3gb_dtype dtype, void* stream) {
