@@ -58,6 +58,12 @@ int grid_for(const void* kernel, int block, int64_t per_block, int64_t units) {
     const int64_t need = (units + per_block - 1) / per_block;
     return int(need < cap ? need : cap);
 }
+int sm_count() {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
 }  // namespace e3gb
 
 using namespace e3gb;

@@ -1,0 +1,578 @@
+// Convolution kernels for 128 channels with per-warp asynchronous prefetch.
+//
+// Every warp works alone on one receiver (forward, "e3j ...", Alg. 2: receiver-stationary
+// accumulation) or one sender (backward, the transposed graph of Eq. 16), with all 128
+// channels (4 per lane) and every output row in registers, exactly like the plain kernels in
+// kernels.cuh. What changes is how operands arrive: the warp walks a flat sequence of
+// "items" (pieces of its edges) and keeps the next NSLOT-1 items in flight in a private
+// shared-memory ring with cp.async, each lane copying the 16-byte channel slice it will
+// itself read. No warp ever waits for another warp, all warps run the same code, and the
+// bytes in flight per SM are (warps per SM) x (NSLOT-1) items regardless of registers.
+//
+//   forward items per edge:   [x rows of the sender + y]  [w rows of paths chunk 0] ...
+//   backward items per sender: [x rows of the sender]; per edge: [y + dm rows + w rows of the
+//                              paths of output block 0] [output block 1] ...
+//
+// Per edge the warp first turns y into the couplings A_p[m3][m1] = sum_m2 C y (a few
+// entries per lane from a recipe table, stored to the warp's shared A buffer); the channel
+// loops then read A as broadcast float4 loads. A sequence position i always uses ring slot
+// i % NSLOT; the issue of item i + NSLOT - 1 overwrites the slot of item i - 1, which this
+// lane has finished reading.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace e3gb {
+
+constexpr int kPipeNq = 128;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte (fp32 x4) or 8-byte (bf16 x4) asynchronous copy of one lane's channel slice
+template <class T>
+__device__ __forceinline__ void cp_async_slice(void* dst, const void* src);
+template <>
+__device__ __forceinline__ void cp_async_slice<float>(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+template <>
+__device__ __forceinline__ void cp_async_slice<__nv_bfloat16>(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <class T>
+__device__ __forceinline__ void lds4(const T* p, float (&o)[4]);
+template <>
+__device__ __forceinline__ void lds4<float>(const float* p, float (&o)[4]) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+}
+template <>
+__device__ __forceinline__ void lds4<__nv_bfloat16>(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 t = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+
+// ------------------------------------------------------------------------------------------
+// compile-time plan
+// ------------------------------------------------------------------------------------------
+template <class Cfg>
+struct PipePlan {
+    // A entries of path p at apos[p] (a multiple of 4 floats) in the warp's A buffer
+    static constexpr std::array<int, Cfg::NP + 1> apos = [] {
+        std::array<int, Cfg::NP + 1> a{};
+        for (int p = 0; p < Cfg::NP; ++p) {
+            const int na = Off<Cfg>::a[p + 1] - Off<Cfg>::a[p];
+            a[p + 1] = a[p] + (na + 3) / 4 * 4;
+        }
+        return a;
+    }();
+    static constexpr int NAPAD = apos[Cfg::NP];
+    // forward: w rows in NWC chunks of PPC paths
+    static constexpr int PPC = 6;
+    static constexpr int NWC = (Cfg::NP + PPC - 1) / PPC;
+    // backward: the paths of each output block, in path order
+    static constexpr std::array<int, Cfg::NOUT + 1> bpos = [] {   // offsets into bpath
+        std::array<int, Cfg::NOUT + 1> o{};
+        for (int p = 0; p < Cfg::NP; ++p) o[Cfg::table.paths[p].out_block + 1]++;
+        for (int j = 0; j < Cfg::NOUT; ++j) o[j + 1] += o[j];
+        return o;
+    }();
+    static constexpr std::array<int, Cfg::NP> bpath = [] {
+        std::array<int, Cfg::NP> b{};
+        int fill[Cfg::NOUT + 1] = {};
+        for (int p = 0; p < Cfg::NP; ++p) {
+            const int j = Cfg::table.paths[p].out_block;
+            b[bpos[j] + fill[j]++] = p;
+        }
+        return b;
+    }();
+    static constexpr int max_block_rows = [] {
+        int m = 0;
+        for (int j = 0; j < Cfg::NOUT; ++j) {
+            const int r = (2 * Cfg::table.outs[j].l + 1) + (bpos[j + 1] - bpos[j]);
+            m = r > m ? r : m;
+        }
+        return m;
+    }();
+};
+
+// one A entry: A[pos] = c0 y[i0] (+ c1 y[i1])
+struct alignas(16) Recipe {
+    float c0, c1;
+    int idx;   // i0 | i1 << 8 | nterms << 16
+    int pos;
+};
+template <class Cfg>
+struct RecipeTable {
+    Recipe r[Cfg::NA];
+};
+template <class Cfg>
+constexpr RecipeTable<Cfg> make_recipes() {
+    RecipeTable<Cfg> t{};
+    for (int p = 0; p < Cfg::NP; ++p) {
+        const int a0 = Off<Cfg>::a[p];
+        const int yo = Cfg::table.paths[p].yoff;
+        for (int k = a0; k < Off<Cfg>::a[p + 1]; ++k) {
+            const AEnt& e = Cfg::aents[k];
+            Recipe r{};
+            r.c0 = e.c[0];
+            r.c1 = e.nt > 1 ? e.c[1] : 0.f;
+            r.idx = (yo + e.m2[0]) | ((yo + (e.nt > 1 ? e.m2[1] : e.m2[0])) << 8) | (e.nt << 16);
+            r.pos = PipePlan<Cfg>::apos[p] + (k - a0);
+            t.r[k] = r;
+        }
+    }
+    return t;
+}
+template <class Cfg>
+__device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg>();
+
+// A entries of one edge, built by the 32 lanes of a warp from y in shared memory
+template <class Cfg, class T>
+__device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float* __restrict__ sA, int lane) {
+#pragma unroll 2
+    for (int i = lane; i < Cfg::NA; i += 32) {
+        const Recipe r = kRecipes<Cfg>.r[i];
+        const int i0 = r.idx & 0xff, i1 = (r.idx >> 8) & 0xff;
+        float v = r.c0 * float(sy[i0]);
+        if ((r.idx >> 16) > 1) v = fmaf(r.c1, float(sy[i1]), v);
+        sA[r.pos] = v;
+    }
+}
+
+// acc[ZOFF + m3][c] += w[c] sum_m1 A[m3][m1] x[xoff + m1][c] for path P; A from shared
+template <class Cfg, int P>
+__device__ __forceinline__ void fwd_path(const float* __restrict__ sA, const float (&xv)[Cfg::D1][kVec],
+                                         const float (&wv)[kVec], float (&acc)[Cfg::D][kVec]) {
+    constexpr PathInfo pi = Cfg::table.paths[P];
+    constexpr int a0 = Off<Cfg>::a[P];
+    constexpr int na = Off<Cfg>::a[P + 1] - a0;
+    constexpr int base = PipePlan<Cfg>::apos[P];
+    constexpr int n1 = 2 * pi.l1 + 1, n3 = 2 * pi.l3 + 1;
+    constexpr int Z = pi.zoff;
+    if constexpr (n1 <= n3) {
+        float xw[n1][kVec];
+#pragma unroll
+        for (int m = 0; m < n1; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) xw[m][c] = xv[pi.xoff + m][c] * wv[c];
+        sfor<(na + 3) / 4>([&](auto qq) {
+            constexpr int q = decltype(qq)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
+            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
+                if constexpr (kk < na) {
+                    constexpr AEnt e = Cfg::aents[a0 + kk];
+#pragma unroll
+                    for (int c = 0; c < kVec; ++c)
+                        acc[Z + e.m3][c] = fmaf(av[decltype(cc)::value], xw[e.m1][c], acc[Z + e.m3][c]);
+                }
+            });
+        });
+    } else {
+        float t[n3][kVec];
+#pragma unroll
+        for (int m = 0; m < n3; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) t[m][c] = 0.f;
+        sfor<(na + 3) / 4>([&](auto qq) {
+            constexpr int q = decltype(qq)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
+            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
+                if constexpr (kk < na) {
+                    constexpr AEnt e = Cfg::aents[a0 + kk];
+#pragma unroll
+                    for (int c = 0; c < kVec; ++c)
+                        t[e.m3][c] = fmaf(av[decltype(cc)::value], xv[pi.xoff + e.m1][c], t[e.m3][c]);
+                }
+            });
+        });
+#pragma unroll
+        for (int m = 0; m < n3; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[Z + m][c] = fmaf(wv[c], t[m][c], acc[Z + m][c]);
+    }
+}
+
+__device__ __forceinline__ bool seg_ok(int64_t k0, int64_t k1, int64_t E) { return k0 >= 0 && k1 >= k0 && k1 <= E; }
+
+// ------------------------------------------------------------------------------------------
+// forward
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T, int NSLOT>
+struct FwdPipe {
+    using PP = PipePlan<Cfg>;
+    static constexpr int NCH = 1 + PP::NWC;                       // items per edge
+    static constexpr int ROWB = kPipeNq * sizeof(T);              // bytes of one 128-channel row
+    static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
+    static constexpr int ROWS = Cfg::D1 > PP::PPC ? Cfg::D1 : PP::PPC;
+    static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
+};
+
+template <class Cfg, class T, int NSLOT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ sender,
+                         const T* __restrict__ x, const T* __restrict__ y, const T* __restrict__ w, float scale,
+                         float* __restrict__ m, unsigned* __restrict__ err) {
+    using F = FwdPipe<Cfg, T, NSLOT>;
+    using PP = PipePlan<Cfg>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    unsigned char* wsm = smem + wid * F::WARP_BYTES;
+    float* sA = reinterpret_cast<float*>(wsm + NSLOT * F::SLOT);
+    const int c0 = lane * kVec;
+    const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
+    const int64_t nw = int64_t(gridDim.x) * WARPS;
+
+    // producer cursor: next item to issue = (edge pe of node pn, chunk pc)
+    int64_t pn = gw, pe = 0, pend = 0;
+    int pc = 0;
+    bool pdone = false;
+    auto p_seek = [&]() {   // make pe < pend or set pdone
+        while (pe >= pend) {
+            if (pn >= N) { pdone = true; return; }
+            const int64_t k0 = __ldg(rowptr + pn), k1 = __ldg(rowptr + pn + 1);
+            pn += nw;
+            if (seg_ok(k0, k1, E)) { pe = k0; pend = k1; }
+        }
+    };
+    auto issue = [&](int64_t i) {   // issue the producer's current item into slot i % NSLOT
+        if (!pdone) {
+            unsigned char* slot = wsm + int(i % NSLOT) * F::SLOT;
+            if (pc == 0) {
+                const int64_t a = __ldg(sender + pe);
+                if (a >= 0 && a < N) {
+#pragma unroll
+                    for (int r = 0; r < Cfg::D1; ++r)
+                        cp_async_slice<T>(slot + r * F::ROWB + c0 * sizeof(T), x + (a * Cfg::D1 + r) * kPipeNq + c0);
+                }
+                if (lane < F::YB / 16) cp_async16(slot + Cfg::D1 * F::ROWB + lane * 16,
+                                                   reinterpret_cast<const unsigned char*>(y + pe * Cfg::D2) + lane * 16);
+            } else {
+                const int p0 = (pc - 1) * PP::PPC;
+                const int np = (Cfg::NP - p0) < PP::PPC ? (Cfg::NP - p0) : PP::PPC;
+                const T* src = w + (pe * Cfg::NP + p0) * kPipeNq + c0;
+#pragma unroll
+                for (int r = 0; r < PP::PPC; ++r)
+                    if (r < np) cp_async_slice<T>(slot + r * F::ROWB + c0 * sizeof(T), src + r * kPipeNq);
+            }
+            if (++pc == F::NCH) {
+                pc = 0;
+                ++pe;
+                p_seek();
+            }
+        }
+        cp_async_commit();
+    };
+    p_seek();
+    int64_t issued = 0;
+    for (int s = 0; s < NSLOT - 1; ++s) issue(issued++);
+
+    int64_t item = 0;
+    for (int64_t b = gw; b < N; b += nw) {
+        int64_t e0 = __ldg(rowptr + b), e1 = __ldg(rowptr + b + 1);
+        if (!seg_ok(e0, e1, E)) {
+            if (lane == 0) atomicOr(err, kErrRowptr);
+            e0 = e1 = 0;
+        }
+        float acc[Cfg::D][kVec];
+#pragma unroll
+        for (int i = 0; i < Cfg::D; ++i)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[i][c] = 0.f;
+        for (int64_t e = e0; e < e1; ++e) {
+            const int64_t a = __ldg(sender + e);
+            const bool ok = a >= 0 && a < N;
+            if (!ok && lane == 0) atomicOr(err, kErrSender);
+            float xv[Cfg::D1][kVec];
+            sfor<F::NCH>([&](auto cc) {
+                constexpr int ch = decltype(cc)::value;
+                issue(issued++);
+                cp_async_wait<NSLOT - 1>();
+                const unsigned char* slot = wsm + int(item % NSLOT) * F::SLOT;
+                ++item;
+                if constexpr (ch == 0) {
+                    __syncwarp();   // y from the lanes that copied it
+                    build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + Cfg::D1 * F::ROWB), sA, lane);
+#pragma unroll
+                    for (int r = 0; r < Cfg::D1; ++r) {
+                        if (ok) lds4<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0, xv[r]);
+                        else
+#pragma unroll
+                            for (int c = 0; c < kVec; ++c) xv[r][c] = 0.f;
+                    }
+                    __syncwarp();   // A visible to every lane
+                } else {
+                    constexpr int p0 = (ch - 1) * PP::PPC;
+                    constexpr int np = (Cfg::NP - p0) < PP::PPC ? (Cfg::NP - p0) : PP::PPC;
+                    sfor<np>([&](auto rr) {
+                        constexpr int r = decltype(rr)::value;
+                        float wv[kVec];
+                        lds4<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0, wv);
+                        fwd_path<Cfg, p0 + r>(sA, xv, wv, acc);
+                    });
+                    if constexpr (ch == F::NCH - 1) __syncwarp();   // A is rebuilt for the next edge
+                }
+            });
+        }
+        float* mb = m + b * (Cfg::D * kPipeNq);
+#pragma unroll
+        for (int i = 0; i < Cfg::D; ++i) {
+            float v[4];
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) v[c] = acc[i][c] * scale;
+            IO<float>::store4(mb + i * kPipeNq + c0, v);
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------------------------------
+// backward (sender order)
+// ------------------------------------------------------------------------------------------
+template <class Cfg, class T, int NSLOT>
+struct BwdPipe {
+    using PP = PipePlan<Cfg>;
+    static constexpr int ROWB = kPipeNq * sizeof(T);
+    static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
+    static constexpr int ROWS = Cfg::D1 > PP::max_block_rows ? Cfg::D1 : PP::max_block_rows;
+    static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
+    static constexpr int NCH = Cfg::NOUT;   // items per edge (one per output block)
+};
+
+// the part of an edge's backward that belongs to output block J; g rows from the slot
+template <class Cfg, class T, int J>
+__device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float* __restrict__ sA,
+                                          const float (&xv)[Cfg::D1][kVec], float (&dxa)[Cfg::D1][kVec],
+                                          float (&dyp)[Cfg::D2], float scale, float* __restrict__ dw_e, int c0) {
+    using PP = PipePlan<Cfg>;
+    constexpr int ROWB = kPipeNq * sizeof(T);
+    constexpr int nrow = 2 * Cfg::table.outs[J].l + 1;
+    constexpr int npb = PP::bpos[J + 1] - PP::bpos[J];
+    float g[nrow][kVec];
+#pragma unroll
+    for (int mm = 0; mm < nrow; ++mm) {
+        lds4<T>(reinterpret_cast<const T*>(slot + mm * ROWB) + c0, g[mm]);
+#pragma unroll
+        for (int c = 0; c < kVec; ++c) g[mm][c] *= scale;
+    }
+    sfor<npb>([&](auto ii) {
+        constexpr int p = PP::bpath[PP::bpos[J] + decltype(ii)::value];
+        constexpr PathInfo pi = Cfg::table.paths[p];
+        constexpr int a0 = Off<Cfg>::a[p];
+        constexpr int na = Off<Cfg>::a[p + 1] - a0;
+        constexpr int n1 = 2 * pi.l1 + 1;
+        constexpr int base = PP::apos[p];
+        float wv[kVec];
+        lds4<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0, wv);
+        float gp[n1][kVec], xw[n1][kVec];
+#pragma unroll
+        for (int mm = 0; mm < n1; ++mm)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) {
+                gp[mm][c] = 0.f;
+                xw[mm][c] = xv[pi.xoff + mm][c] * wv[c];
+            }
+        sfor<(na + 3) / 4>([&](auto qq) {
+            constexpr int q = decltype(qq)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
+            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
+                if constexpr (kk < na) {
+                    constexpr AEnt e = Cfg::aents[a0 + kk];
+                    float s = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kVec; ++c) {
+                        gp[e.m1][c] = fmaf(av[decltype(cc)::value], g[e.m3][c], gp[e.m1][c]);
+                        s = fmaf(xw[e.m1][c], g[e.m3][c], s);
+                    }
+                    sfor<e.nt>([&](auto t) {
+                        constexpr int tt = decltype(t)::value;
+                        dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
+                    });
+                }
+            });
+        });
+        float dwv[kVec];
+#pragma unroll
+        for (int c = 0; c < kVec; ++c) {
+            float s = 0.f;
+#pragma unroll
+            for (int mm = 0; mm < n1; ++mm) {
+                s = fmaf(xv[pi.xoff + mm][c], gp[mm][c], s);
+                dxa[pi.xoff + mm][c] = fmaf(wv[c], gp[mm][c], dxa[pi.xoff + mm][c]);
+            }
+            dwv[c] = s;
+        }
+        __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0), make_float4(dwv[0], dwv[1], dwv[2], dwv[3]));
+    });
+}
+
+template <class Cfg, class T, int NSLOT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr, const int32_t* __restrict__ cedge,
+                          const int32_t* __restrict__ crecv, const T* __restrict__ x, const T* __restrict__ y,
+                          const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
+                          float* __restrict__ dy, float* __restrict__ dw, unsigned* __restrict__ err) {
+    using B = BwdPipe<Cfg, T, NSLOT>;
+    using PP = PipePlan<Cfg>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    unsigned char* wsm = smem + wid * B::WARP_BYTES;
+    float* sA = reinterpret_cast<float*>(wsm + NSLOT * B::SLOT);
+    const int c0 = lane * kVec;
+    const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
+    const int64_t nw = int64_t(gridDim.x) * WARPS;
+
+    // producer cursor: sender pa, edge position pk in [pk, pkend), item pc (-1: x rows of pa)
+    int64_t pa = gw - nw, pk = 0, pkend = 0;
+    int pc = 0;
+    bool pdone = false;
+    auto p_next_sender = [&]() {
+        pa += nw;
+        if (pa >= N) { pdone = true; return; }
+        int64_t k0 = __ldg(cptr + pa), k1 = __ldg(cptr + pa + 1);
+        if (!seg_ok(k0, k1, E)) k0 = k1 = 0;
+        pk = k0;
+        pkend = k1;
+        pc = -1;
+    };
+    auto issue = [&](int64_t i) {
+        if (!pdone) {
+            unsigned char* slot = wsm + int(i % NSLOT) * B::SLOT;
+            if (pc < 0) {   // x rows of the sender
+#pragma unroll
+                for (int r = 0; r < Cfg::D1; ++r)
+                    cp_async_slice<T>(slot + r * B::ROWB + c0 * sizeof(T), x + (pa * Cfg::D1 + r) * kPipeNq + c0);
+                pc = 0;
+                if (pk >= pkend) p_next_sender();
+            } else {
+                const int64_t e = __ldg(cedge + pk), bb = __ldg(crecv + pk);
+                const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
+                if (ok) {
+                    // rows of output block pc: dm rows, then w rows of its paths; y behind them
+                    sfor<Cfg::NOUT>([&](auto jj) {
+                        constexpr int j = decltype(jj)::value;
+                        if (pc == j) {
+                            constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
+                            constexpr int zo = Off<Cfg>::z[j];
+#pragma unroll
+                            for (int r = 0; r < nrow; ++r)
+                                cp_async_slice<T>(slot + r * B::ROWB + c0 * sizeof(T),
+                                                  dm + (bb * Cfg::D + zo + r) * kPipeNq + c0);
+                            sfor<PP::bpos[j + 1] - PP::bpos[j]>([&](auto ii) {
+                                constexpr int p = PP::bpath[PP::bpos[j] + decltype(ii)::value];
+                                cp_async_slice<T>(slot + (nrow + decltype(ii)::value) * B::ROWB + c0 * sizeof(T),
+                                                  w + (e * Cfg::NP + p) * kPipeNq + c0);
+                            });
+                        }
+                    });
+                    if (pc == 0 && lane < B::YB / 16)
+                        cp_async16(slot + B::ROWS * B::ROWB + lane * 16,
+                                   reinterpret_cast<const unsigned char*>(y + e * Cfg::D2) + lane * 16);
+                }
+                if (++pc == B::NCH) {
+                    pc = 0;
+                    if (++pk >= pkend) p_next_sender();
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    p_next_sender();
+    int64_t issued = 0;
+    for (int s = 0; s < NSLOT - 1; ++s) issue(issued++);
+
+    int64_t item = 0;
+    for (int64_t a = gw; a < N; a += nw) {
+        int64_t k0 = __ldg(cptr + a), k1 = __ldg(cptr + a + 1);
+        if (!seg_ok(k0, k1, E)) {
+            if (lane == 0) atomicOr(err, kErrRowptr);
+            k0 = k1 = 0;
+        }
+        float xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec];
+        {   // item: x rows of the sender
+            issue(issued++);
+            cp_async_wait<NSLOT - 1>();
+            const unsigned char* slot = wsm + int(item % NSLOT) * B::SLOT;
+            ++item;
+#pragma unroll
+            for (int r = 0; r < Cfg::D1; ++r) {
+                lds4<T>(reinterpret_cast<const T*>(slot + r * B::ROWB) + c0, xv[r]);
+#pragma unroll
+                for (int c = 0; c < kVec; ++c) dxa[r][c] = 0.f;
+            }
+        }
+        for (int64_t k = k0; k < k1; ++k) {
+            const int64_t e = __ldg(cedge + k), bb = __ldg(crecv + k);
+            const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
+            if (!ok && lane == 0) atomicOr(err, kErrRecv);
+            float dyp[Cfg::D2];
+#pragma unroll
+            for (int t = 0; t < Cfg::D2; ++t) dyp[t] = 0.f;
+            float* dw_e = dw + (ok ? e : 0) * (Cfg::NP * kPipeNq);
+            sfor<B::NCH>([&](auto jj) {
+                constexpr int j = decltype(jj)::value;
+                issue(issued++);
+                cp_async_wait<NSLOT - 1>();
+                const unsigned char* slot = wsm + int(item % NSLOT) * B::SLOT;
+                ++item;
+                if constexpr (j == 0) {
+                    __syncwarp();
+                    if (ok) build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane);
+                    __syncwarp();
+                }
+                if (ok) bwd_block<Cfg, T, j>(slot, sA, xv, dxa, dyp, scale, dw_e, c0);
+                if constexpr (j == B::NCH - 1) __syncwarp();
+            });
+            group_reduce<Cfg::D2>(dyp, 32);
+            if (ok && lane < Cfg::D2) {
+                float v = 0.f;
+#pragma unroll
+                for (int t = 0; t < Cfg::D2; ++t) v = lane == t ? dyp[t] : v;
+                dy[e * Cfg::D2 + lane] = v;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < Cfg::D1; ++r) IO<float>::store4(dx + (a * Cfg::D1 + r) * kPipeNq + c0, dxa[r]);
+    }
+    cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------------------------------
+// launch shapes
+// ------------------------------------------------------------------------------------------
+constexpr int kSmemLimit = 232448;   // 227 KiB per block
+
+template <class Cfg, class T, bool BWD>
+struct PipeShape {
+    static constexpr int NSLOT = BWD ? 3 : 4;
+    static constexpr int WARP_BYTES = BWD ? BwdPipe<Cfg, T, NSLOT>::WARP_BYTES : FwdPipe<Cfg, T, NSLOT>::WARP_BYTES;
+    static constexpr int by_smem = kSmemLimit / WARP_BYTES;
+    static constexpr int WARPS = by_smem < 8 ? by_smem : 8;
+    static constexpr int SMEM = WARPS * WARP_BYTES;
+    static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4;
+};
+
+}  // namespace e3gb

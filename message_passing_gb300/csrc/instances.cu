@@ -1,5 +1,6 @@
 // One irreps configuration's kernels and launchers; compiled once per entry of configs.def
 // with -DE3GB_CFG=<id>, each unit exporting e3gb::ops_<id>().
+#include "conv_pipe.cuh"
 #include "kernels.cuh"
 
 #ifndef E3GB_CFG
@@ -52,9 +53,25 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
     return cudaGetLastError();
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
                      const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s) {
+    using S = PipeShape<Cfg, T, false>;
+    if constexpr (S::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w)) {
+            auto k = conv_forward_pipe_kernel<Cfg, T, S::NSLOT, S::WARPS>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t need = (N + S::WARPS - 1) / S::WARPS;
+            const int grid = int(sm_count() < need ? sm_count() : need);
+            if (grid == 0) return cudaSuccess;
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale,
+                                                   (float*)m, err);
+            return cudaGetLastError();
+        }
+    }
     auto k = conv_forward_kernel<Cfg, T>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
@@ -67,6 +84,20 @@ template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
                      void* dw, unsigned* err, cudaStream_t s) {
+    using S = PipeShape<Cfg, T, true>;
+    if constexpr (S::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm)) {
+            auto k = conv_backward_pipe_kernel<Cfg, T, S::NSLOT, S::WARPS>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t need = (N + S::WARPS - 1) / S::WARPS;
+            const int grid = int(sm_count() < need ? sm_count() : need);
+            if (grid == 0) return cudaSuccess;
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
+                                                   (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, err);
+            return cudaGetLastError();
+        }
+    }
     auto k = conv_backward_kernel<Cfg, T>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;

@@ -516,5 +516,6 @@ struct ConfigOps {
 };
 
 int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units);
+int sm_count();
 
 }  // namespace e3gb
