@@ -140,23 +140,41 @@ constexpr RecipeTable<Cfg> make_recipes() {
 template <class Cfg>
 __device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg>();
 
-// A entries of one edge, built by the 32 lanes of a warp from y in shared memory
+// A entries of one edge, built by the 32 lanes of a warp from y in shared memory. Each
+// entry is stored twice, (A, A), so that a 16-byte load yields two ready operand pairs for
+// the paired (f32x2) multiply-adds of the channel loops.
 template <class Cfg, class T>
-__device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float* __restrict__ sA, int lane) {
+__device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float2* __restrict__ sA, int lane) {
 #pragma unroll 2
     for (int i = lane; i < Cfg::NA; i += 32) {
         const Recipe r = kRecipes<Cfg>.r[i];
         const int i0 = r.idx & 0xff, i1 = (r.idx >> 8) & 0xff;
         float v = r.c0 * float(sy[i0]);
         if ((r.idx >> 16) > 1) v = fmaf(r.c1, float(sy[i1]), v);
-        sA[r.pos] = v;
+        sA[r.pos] = make_float2(v, v);
     }
 }
 
-// acc[ZOFF + m3][c] += w[c] sum_m1 A[m3][m1] x[xoff + m1][c] for path P; A from shared
+// channel quads as two pairs
+struct Q2 {
+    float2 lo, hi;
+};
+__device__ __forceinline__ Q2 q2_of(const float (&v)[4]) { return {make_float2(v[0], v[1]), make_float2(v[2], v[3])}; }
+__device__ __forceinline__ Q2 q2_mul(Q2 a, Q2 b) { return {__fmul2_rn(a.lo, b.lo), __fmul2_rn(a.hi, b.hi)}; }
+__device__ __forceinline__ Q2 q2_fma(float2 a, Q2 b, Q2 c) { return {__ffma2_rn(a, b.lo, c.lo), __ffma2_rn(a, b.hi, c.hi)}; }
+__device__ __forceinline__ Q2 q2_fma(Q2 a, Q2 b, Q2 c) { return {__ffma2_rn(a.lo, b.lo, c.lo), __ffma2_rn(a.hi, b.hi, c.hi)}; }
+__device__ __forceinline__ Q2 q2_zero() { return {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}; }
+template <class T>
+__device__ __forceinline__ Q2 lds_q2(const T* p) {
+    float v[4];
+    lds4<T>(p, v);
+    return q2_of(v);
+}
+
+// acc[Z + m3] += w * sum_m1 A[m3][m1] x[xoff + m1] for path P (4 channels as two pairs)
 template <class Cfg, int P>
-__device__ __forceinline__ void fwd_path(const float* __restrict__ sA, const float (&xv)[Cfg::D1][kVec],
-                                         const float (&wv)[kVec], float (&acc)[Cfg::D][kVec]) {
+__device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2 (&xv)[Cfg::D1], Q2 wv,
+                                         Q2 (&acc)[Cfg::D]) {
     constexpr PathInfo pi = Cfg::table.paths[P];
     constexpr int a0 = Off<Cfg>::a[P];
     constexpr int na = Off<Cfg>::a[P + 1] - a0;
@@ -164,49 +182,39 @@ __device__ __forceinline__ void fwd_path(const float* __restrict__ sA, const flo
     constexpr int n1 = 2 * pi.l1 + 1, n3 = 2 * pi.l3 + 1;
     constexpr int Z = pi.zoff;
     if constexpr (n1 <= n3) {
-        float xw[n1][kVec];
+        Q2 xw[n1];
 #pragma unroll
-        for (int m = 0; m < n1; ++m)
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) xw[m][c] = xv[pi.xoff + m][c] * wv[c];
-        sfor<(na + 3) / 4>([&](auto qq) {
+        for (int m = 0; m < n1; ++m) xw[m] = q2_mul(xv[pi.xoff + m], wv);
+        sfor<(na + 1) / 2>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
-            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
-            sfor<4>([&](auto cc) {
-                constexpr int kk = 4 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
+            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
+            sfor<2>([&](auto cc) {
+                constexpr int kk = 2 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
-#pragma unroll
-                    for (int c = 0; c < kVec; ++c)
-                        acc[Z + e.m3][c] = fmaf(av[decltype(cc)::value], xw[e.m1][c], acc[Z + e.m3][c]);
+                    acc[Z + e.m3] = q2_fma(av[decltype(cc)::value], xw[e.m1], acc[Z + e.m3]);
                 }
             });
         });
     } else {
-        float t[n3][kVec];
+        Q2 t[n3];
 #pragma unroll
-        for (int m = 0; m < n3; ++m)
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) t[m][c] = 0.f;
-        sfor<(na + 3) / 4>([&](auto qq) {
+        for (int m = 0; m < n3; ++m) t[m] = q2_zero();
+        sfor<(na + 1) / 2>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
-            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
-            sfor<4>([&](auto cc) {
-                constexpr int kk = 4 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
+            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
+            sfor<2>([&](auto cc) {
+                constexpr int kk = 2 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
-#pragma unroll
-                    for (int c = 0; c < kVec; ++c)
-                        t[e.m3][c] = fmaf(av[decltype(cc)::value], xv[pi.xoff + e.m1][c], t[e.m3][c]);
+                    t[e.m3] = q2_fma(av[decltype(cc)::value], xv[pi.xoff + e.m1], t[e.m3]);
                 }
             });
         });
 #pragma unroll
-        for (int m = 0; m < n3; ++m)
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) acc[Z + m][c] = fmaf(wv[c], t[m][c], acc[Z + m][c]);
+        for (int m = 0; m < n3; ++m) acc[Z + m] = q2_fma(wv, t[m], acc[Z + m]);
     }
 }
 
@@ -223,7 +231,7 @@ struct FwdPipe {
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWS = Cfg::D1 > PP::PPC ? Cfg::D1 : PP::PPC;
     static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8;
 };
 
 template <class Cfg, class T, int NSLOT, int WARPS>
@@ -237,7 +245,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     unsigned char* wsm = smem + wid * F::WARP_BYTES;
-    float* sA = reinterpret_cast<float*>(wsm + NSLOT * F::SLOT);
+    float2* sA = reinterpret_cast<float2*>(wsm + NSLOT * F::SLOT);
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
     const int64_t nw = int64_t(gridDim.x) * WARPS;
@@ -293,16 +301,14 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
             if (lane == 0) atomicOr(err, kErrRowptr);
             e0 = e1 = 0;
         }
-        float acc[Cfg::D][kVec];
+        Q2 acc[Cfg::D];
 #pragma unroll
-        for (int i = 0; i < Cfg::D; ++i)
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) acc[i][c] = 0.f;
+        for (int i = 0; i < Cfg::D; ++i) acc[i] = q2_zero();
         for (int64_t e = e0; e < e1; ++e) {
             const int64_t a = __ldg(sender + e);
             const bool ok = a >= 0 && a < N;
             if (!ok && lane == 0) atomicOr(err, kErrSender);
-            float xv[Cfg::D1][kVec];
+            Q2 xv[Cfg::D1];
             sfor<F::NCH>([&](auto cc) {
                 constexpr int ch = decltype(cc)::value;
                 issue(issued++);
@@ -313,20 +319,15 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
                     __syncwarp();   // y from the lanes that copied it
                     build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + Cfg::D1 * F::ROWB), sA, lane);
 #pragma unroll
-                    for (int r = 0; r < Cfg::D1; ++r) {
-                        if (ok) lds4<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0, xv[r]);
-                        else
-#pragma unroll
-                            for (int c = 0; c < kVec; ++c) xv[r][c] = 0.f;
-                    }
+                    for (int r = 0; r < Cfg::D1; ++r)
+                        xv[r] = ok ? lds_q2<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0) : q2_zero();
                     __syncwarp();   // A visible to every lane
                 } else {
                     constexpr int p0 = (ch - 1) * PP::PPC;
                     constexpr int np = (Cfg::NP - p0) < PP::PPC ? (Cfg::NP - p0) : PP::PPC;
                     sfor<np>([&](auto rr) {
                         constexpr int r = decltype(rr)::value;
-                        float wv[kVec];
-                        lds4<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0, wv);
+                        const Q2 wv = lds_q2<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0);
                         fwd_path<Cfg, p0 + r>(sA, xv, wv, acc);
                     });
                     if constexpr (ch == F::NCH - 1) __syncwarp();   // A is rebuilt for the next edge
@@ -334,12 +335,11 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
             });
         }
         float* mb = m + b * (Cfg::D * kPipeNq);
+        const float2 sc = make_float2(scale, scale);
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i) {
-            float v[4];
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) v[c] = acc[i][c] * scale;
-            IO<float>::store4(mb + i * kPipeNq + c0, v);
+            const float2 lo = __fmul2_rn(acc[i].lo, sc), hi = __fmul2_rn(acc[i].hi, sc);
+            *reinterpret_cast<float4*>(mb + i * kPipeNq + c0) = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     }
     cp_async_wait<0>();
@@ -355,25 +355,24 @@ struct BwdPipe {
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWS = Cfg::D1 > PP::max_block_rows ? Cfg::D1 : PP::max_block_rows;
     static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8;
     static constexpr int NCH = Cfg::NOUT;   // items per edge (one per output block)
 };
 
 // the part of an edge's backward that belongs to output block J; g rows from the slot
 template <class Cfg, class T, int J>
-__device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float* __restrict__ sA,
-                                          const float (&xv)[Cfg::D1][kVec], float (&dxa)[Cfg::D1][kVec],
-                                          float (&dyp)[Cfg::D2], float scale, float* __restrict__ dw_e, int c0) {
+__device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float2* __restrict__ sA,
+                                          const Q2 (&xv)[Cfg::D1], Q2 (&dxa)[Cfg::D1], float (&dyp)[Cfg::D2],
+                                          float2 sc, float* __restrict__ dw_e, int c0) {
     using PP = PipePlan<Cfg>;
     constexpr int ROWB = kPipeNq * sizeof(T);
     constexpr int nrow = 2 * Cfg::table.outs[J].l + 1;
     constexpr int npb = PP::bpos[J + 1] - PP::bpos[J];
-    float g[nrow][kVec];
+    Q2 g[nrow];
 #pragma unroll
     for (int mm = 0; mm < nrow; ++mm) {
-        lds4<T>(reinterpret_cast<const T*>(slot + mm * ROWB) + c0, g[mm]);
-#pragma unroll
-        for (int c = 0; c < kVec; ++c) g[mm][c] *= scale;
+        const Q2 v = lds_q2<T>(reinterpret_cast<const T*>(slot + mm * ROWB) + c0);
+        g[mm] = {__fmul2_rn(v.lo, sc), __fmul2_rn(v.hi, sc)};
     }
     sfor<npb>([&](auto ii) {
         constexpr int p = PP::bpath[PP::bpos[J] + decltype(ii)::value];
@@ -382,30 +381,25 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
         constexpr int na = Off<Cfg>::a[p + 1] - a0;
         constexpr int n1 = 2 * pi.l1 + 1;
         constexpr int base = PP::apos[p];
-        float wv[kVec];
-        lds4<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0, wv);
-        float gp[n1][kVec], xw[n1][kVec];
+        const Q2 wv = lds_q2<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0);
+        Q2 gp[n1], xw[n1];
 #pragma unroll
-        for (int mm = 0; mm < n1; ++mm)
-#pragma unroll
-            for (int c = 0; c < kVec; ++c) {
-                gp[mm][c] = 0.f;
-                xw[mm][c] = xv[pi.xoff + mm][c] * wv[c];
-            }
-        sfor<(na + 3) / 4>([&](auto qq) {
+        for (int mm = 0; mm < n1; ++mm) {
+            gp[mm] = q2_zero();
+            xw[mm] = q2_mul(xv[pi.xoff + mm], wv);
+        }
+        sfor<(na + 1) / 2>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 4 * q);
-            const float av[4] = {t4.x, t4.y, t4.z, t4.w};
-            sfor<4>([&](auto cc) {
-                constexpr int kk = 4 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
+            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
+            sfor<2>([&](auto cc) {
+                constexpr int kk = 2 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
-                    float s = 0.f;
-#pragma unroll
-                    for (int c = 0; c < kVec; ++c) {
-                        gp[e.m1][c] = fmaf(av[decltype(cc)::value], g[e.m3][c], gp[e.m1][c]);
-                        s = fmaf(xw[e.m1][c], g[e.m3][c], s);
-                    }
+                    gp[e.m1] = q2_fma(av[decltype(cc)::value], g[e.m3], gp[e.m1]);
+                    // sum over the lane's 4 channels of x w g, for dy
+                    const float2 s2 = __ffma2_rn(xw[e.m1].hi, g[e.m3].hi, __fmul2_rn(xw[e.m1].lo, g[e.m3].lo));
+                    const float s = s2.x + s2.y;
                     sfor<e.nt>([&](auto t) {
                         constexpr int tt = decltype(t)::value;
                         dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
@@ -413,18 +407,13 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
                 }
             });
         });
-        float dwv[kVec];
+        Q2 dwv = q2_zero();
 #pragma unroll
-        for (int c = 0; c < kVec; ++c) {
-            float s = 0.f;
-#pragma unroll
-            for (int mm = 0; mm < n1; ++mm) {
-                s = fmaf(xv[pi.xoff + mm][c], gp[mm][c], s);
-                dxa[pi.xoff + mm][c] = fmaf(wv[c], gp[mm][c], dxa[pi.xoff + mm][c]);
-            }
-            dwv[c] = s;
+        for (int mm = 0; mm < n1; ++mm) {
+            dwv = q2_fma(xv[pi.xoff + mm], gp[mm], dwv);
+            dxa[pi.xoff + mm] = q2_fma(wv, gp[mm], dxa[pi.xoff + mm]);
         }
-        __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0), make_float4(dwv[0], dwv[1], dwv[2], dwv[3]));
+        __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0), make_float4(dwv.lo.x, dwv.lo.y, dwv.hi.x, dwv.hi.y));
     });
 }
 
@@ -440,7 +429,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     unsigned char* wsm = smem + wid * B::WARP_BYTES;
-    float* sA = reinterpret_cast<float*>(wsm + NSLOT * B::SLOT);
+    float2* sA = reinterpret_cast<float2*>(wsm + NSLOT * B::SLOT);
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
     const int64_t nw = int64_t(gridDim.x) * WARPS;
@@ -511,7 +500,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             if (lane == 0) atomicOr(err, kErrRowptr);
             k0 = k1 = 0;
         }
-        float xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec];
+        Q2 xv[Cfg::D1], dxa[Cfg::D1];
         {   // item: x rows of the sender
             issue(issued++);
             cp_async_wait<NSLOT - 1>();
@@ -519,11 +508,11 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             ++item;
 #pragma unroll
             for (int r = 0; r < Cfg::D1; ++r) {
-                lds4<T>(reinterpret_cast<const T*>(slot + r * B::ROWB) + c0, xv[r]);
-#pragma unroll
-                for (int c = 0; c < kVec; ++c) dxa[r][c] = 0.f;
+                xv[r] = lds_q2<T>(reinterpret_cast<const T*>(slot + r * B::ROWB) + c0);
+                dxa[r] = q2_zero();
             }
         }
+        const float2 sc = make_float2(scale, scale);
         for (int64_t k = k0; k < k1; ++k) {
             const int64_t e = __ldg(cedge + k), bb = __ldg(crecv + k);
             const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
@@ -543,7 +532,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                     if (ok) build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane);
                     __syncwarp();
                 }
-                if (ok) bwd_block<Cfg, T, j>(slot, sA, xv, dxa, dyp, scale, dw_e, c0);
+                if (ok) bwd_block<Cfg, T, j>(slot, sA, xv, dxa, dyp, sc, dw_e, c0);
                 if constexpr (j == B::NCH - 1) __syncwarp();
             });
             group_reduce<Cfg::D2>(dyp, 32);
@@ -555,7 +544,9 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             }
         }
 #pragma unroll
-        for (int r = 0; r < Cfg::D1; ++r) IO<float>::store4(dx + (a * Cfg::D1 + r) * kPipeNq + c0, dxa[r]);
+        for (int r = 0; r < Cfg::D1; ++r)
+            *reinterpret_cast<float4*>(dx + (a * Cfg::D1 + r) * kPipeNq + c0) =
+                make_float4(dxa[r].lo.x, dxa[r].lo.y, dxa[r].hi.x, dxa[r].hi.y);
     }
     cp_async_wait<0>();
 }
