@@ -80,6 +80,18 @@ struct PipePlan {
         return a;
     }();
     static constexpr int NAPAD = apos[Cfg::NP];
+    // forward order of the A entries inside each path: m1-major, so that consecutive
+    // multiply-adds update different accumulator rows (independent chains)
+    static constexpr std::array<int, Cfg::NA> fwd_order = [] {
+        std::array<int, Cfg::NA> o{};
+        for (int p = 0; p < Cfg::NP; ++p) {
+            int n = Off<Cfg>::a[p];
+            for (int m1 = 0; m1 < 7; ++m1)
+                for (int k = Off<Cfg>::a[p]; k < Off<Cfg>::a[p + 1]; ++k)
+                    if (Cfg::aents[k].m1 == m1) o[n++] = k;
+        }
+        return o;
+    }();
     // forward: w rows in NWC chunks of PPC paths
     static constexpr int PPC = 6;
     static constexpr int NWC = (Cfg::NP + PPC - 1) / PPC;
@@ -119,14 +131,16 @@ template <class Cfg>
 struct RecipeTable {
     Recipe r[Cfg::NA];
 };
-template <class Cfg>
+// FWD: entries placed in forward order (PipePlan::fwd_order), else in table order
+template <class Cfg, bool FWD>
 constexpr RecipeTable<Cfg> make_recipes() {
     RecipeTable<Cfg> t{};
     for (int p = 0; p < Cfg::NP; ++p) {
         const int a0 = Off<Cfg>::a[p];
         const int yo = Cfg::table.paths[p].yoff;
         for (int k = a0; k < Off<Cfg>::a[p + 1]; ++k) {
-            const AEnt& e = Cfg::aents[k];
+            const int src = FWD ? PipePlan<Cfg>::fwd_order[k] : k;
+            const AEnt& e = Cfg::aents[src];
             Recipe r{};
             r.c0 = e.c[0];
             r.c1 = e.nt > 1 ? e.c[1] : 0.f;
@@ -137,17 +151,17 @@ constexpr RecipeTable<Cfg> make_recipes() {
     }
     return t;
 }
-template <class Cfg>
-__device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg>();
+template <class Cfg, bool FWD>
+__device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg, FWD>();
 
 // A entries of one edge, built by the 32 lanes of a warp from y in shared memory. Each
 // entry is stored twice, (A, A), so that a 16-byte load yields two ready operand pairs for
 // the paired (f32x2) multiply-adds of the channel loops.
-template <class Cfg, class T>
+template <class Cfg, bool FWD, class T>
 __device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float2* __restrict__ sA, int lane) {
 #pragma unroll 2
     for (int i = lane; i < Cfg::NA; i += 32) {
-        const Recipe r = kRecipes<Cfg>.r[i];
+        const Recipe r = kRecipes<Cfg, FWD>.r[i];
         const int i0 = r.idx & 0xff, i1 = (r.idx >> 8) & 0xff;
         float v = r.c0 * float(sy[i0]);
         if ((r.idx >> 16) > 1) v = fmaf(r.c1, float(sy[i1]), v);
@@ -192,7 +206,7 @@ __device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2
             sfor<2>([&](auto cc) {
                 constexpr int kk = 2 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
-                    constexpr AEnt e = Cfg::aents[a0 + kk];
+                    constexpr AEnt e = Cfg::aents[PipePlan<Cfg>::fwd_order[a0 + kk]];
                     acc[Z + e.m3] = q2_fma(av[decltype(cc)::value], xw[e.m1], acc[Z + e.m3]);
                 }
             });
@@ -208,7 +222,7 @@ __device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2
             sfor<2>([&](auto cc) {
                 constexpr int kk = 2 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
-                    constexpr AEnt e = Cfg::aents[a0 + kk];
+                    constexpr AEnt e = Cfg::aents[PipePlan<Cfg>::fwd_order[a0 + kk]];
                     t[e.m3] = q2_fma(av[decltype(cc)::value], xv[pi.xoff + e.m1], t[e.m3]);
                 }
             });
@@ -219,6 +233,34 @@ __device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2
 }
 
 __device__ __forceinline__ bool seg_ok(int64_t k0, int64_t k1, int64_t E) { return k0 >= 0 && k1 >= k0 && k1 <= E; }
+
+// Sum each of N (a power of two <= 32) per-lane values over the 32 lanes of the warp with a
+// transposing butterfly: every step halves the values a lane holds (it keeps one half and
+// adds its partner's copy of that half), then plain butterfly steps finish the sum. The
+// 32/N lanes that differ only in their low bits end with the same sum; *index receives
+// which of the N sums this lane holds. Fixed order: deterministic. 16 values: 16 shuffles.
+template <int N>
+__device__ __forceinline__ float warp_sum_transposed(float (&v)[N], int lane, int* index) {
+    static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
+    int idx = 0;
+    sfor<__builtin_ctz(N)>([&](auto ss) {
+        constexpr int st = decltype(ss)::value;
+        constexpr int off = 16 >> st;
+        constexpr int half = N >> (st + 1);
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        idx += upper ? half : 0;
+    });
+#pragma unroll
+    for (int off = 16 >> __builtin_ctz(N); off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    *index = idx;
+    return v[0];
+}
 
 // ------------------------------------------------------------------------------------------
 // forward
@@ -317,7 +359,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
                 ++item;
                 if constexpr (ch == 0) {
                     __syncwarp();   // y from the lanes that copied it
-                    build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + Cfg::D1 * F::ROWB), sA, lane);
+                    build_A_warp<Cfg, true, T>(reinterpret_cast<const T*>(slot + Cfg::D1 * F::ROWB), sA, lane);
 #pragma unroll
                     for (int r = 0; r < Cfg::D1; ++r)
                         xv[r] = ok ? lds_q2<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0) : q2_zero();
@@ -355,14 +397,15 @@ struct BwdPipe {
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWS = Cfg::D1 > PP::max_block_rows ? Cfg::D1 : PP::max_block_rows;
     static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8;
+    static constexpr int XBUF = Cfg::D1 * kPipeNq * 4;            // the sender's x rows (fp32)
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8 + XBUF;
     static constexpr int NCH = Cfg::NOUT;   // items per edge (one per output block)
 };
 
 // the part of an edge's backward that belongs to output block J; g rows from the slot
 template <class Cfg, class T, int J>
 __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float2* __restrict__ sA,
-                                          const Q2 (&xv)[Cfg::D1], Q2 (&dxa)[Cfg::D1], float (&dyp)[Cfg::D2],
+                                          const float* __restrict__ sx, Q2 (&dxa)[Cfg::D1], float (&dyp)[Cfg::D2],
                                           float2 sc, float* __restrict__ dw_e, int c0) {
     using PP = PipePlan<Cfg>;
     constexpr int ROWB = kPipeNq * sizeof(T);
@@ -382,11 +425,12 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
         constexpr int n1 = 2 * pi.l1 + 1;
         constexpr int base = PP::apos[p];
         const Q2 wv = lds_q2<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0);
-        Q2 gp[n1], xw[n1];
+        Q2 gp[n1], xw[n1], xr[n1];
 #pragma unroll
         for (int mm = 0; mm < n1; ++mm) {
+            xr[mm] = lds_q2<float>(sx + (pi.xoff + mm) * kPipeNq + c0);
             gp[mm] = q2_zero();
-            xw[mm] = q2_mul(xv[pi.xoff + mm], wv);
+            xw[mm] = q2_mul(xr[mm], wv);
         }
         sfor<(na + 1) / 2>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
@@ -397,9 +441,11 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
                     gp[e.m1] = q2_fma(av[decltype(cc)::value], g[e.m3], gp[e.m1]);
-                    // sum over the lane's 4 channels of x w g, for dy
-                    const float2 s2 = __ffma2_rn(xw[e.m1].hi, g[e.m3].hi, __fmul2_rn(xw[e.m1].lo, g[e.m3].lo));
-                    const float s = s2.x + s2.y;
+                    // sum over the lane's 4 channels of x w g, for dy (scalar: 4 pipe cycles)
+                    float s = xw[e.m1].lo.x * g[e.m3].lo.x;
+                    s = fmaf(xw[e.m1].lo.y, g[e.m3].lo.y, s);
+                    s = fmaf(xw[e.m1].hi.x, g[e.m3].hi.x, s);
+                    s = fmaf(xw[e.m1].hi.y, g[e.m3].hi.y, s);
                     sfor<e.nt>([&](auto t) {
                         constexpr int tt = decltype(t)::value;
                         dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
@@ -410,7 +456,7 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
         Q2 dwv = q2_zero();
 #pragma unroll
         for (int mm = 0; mm < n1; ++mm) {
-            dwv = q2_fma(xv[pi.xoff + mm], gp[mm], dwv);
+            dwv = q2_fma(xr[mm], gp[mm], dwv);
             dxa[pi.xoff + mm] = q2_fma(wv, gp[mm], dxa[pi.xoff + mm]);
         }
         __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0), make_float4(dwv.lo.x, dwv.lo.y, dwv.hi.x, dwv.hi.y));
@@ -430,6 +476,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
     const int wid = threadIdx.x >> 5;
     unsigned char* wsm = smem + wid * B::WARP_BYTES;
     float2* sA = reinterpret_cast<float2*>(wsm + NSLOT * B::SLOT);
+    float* sx = reinterpret_cast<float*>(wsm + NSLOT * B::SLOT + PP::NAPAD * 8);
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
     const int64_t nw = int64_t(gridDim.x) * WARPS;
@@ -500,15 +547,16 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             if (lane == 0) atomicOr(err, kErrRowptr);
             k0 = k1 = 0;
         }
-        Q2 xv[Cfg::D1], dxa[Cfg::D1];
-        {   // item: x rows of the sender
+        Q2 dxa[Cfg::D1];
+        {   // item: x rows of the sender -> the warp's x buffer (each lane its own channels)
             issue(issued++);
             cp_async_wait<NSLOT - 1>();
             const unsigned char* slot = wsm + int(item % NSLOT) * B::SLOT;
             ++item;
 #pragma unroll
             for (int r = 0; r < Cfg::D1; ++r) {
-                xv[r] = lds_q2<T>(reinterpret_cast<const T*>(slot + r * B::ROWB) + c0);
+                const Q2 v = lds_q2<T>(reinterpret_cast<const T*>(slot + r * B::ROWB) + c0);
+                *reinterpret_cast<float4*>(sx + r * kPipeNq + c0) = make_float4(v.lo.x, v.lo.y, v.hi.x, v.hi.y);
                 dxa[r] = q2_zero();
             }
         }
@@ -529,19 +577,15 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                 ++item;
                 if constexpr (j == 0) {
                     __syncwarp();
-                    if (ok) build_A_warp<Cfg, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane);
+                    if (ok) build_A_warp<Cfg, false, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane);
                     __syncwarp();
                 }
-                if (ok) bwd_block<Cfg, T, j>(slot, sA, xv, dxa, dyp, sc, dw_e, c0);
+                if (ok) bwd_block<Cfg, T, j>(slot, sA, sx, dxa, dyp, sc, dw_e, c0);
                 if constexpr (j == B::NCH - 1) __syncwarp();
             });
-            group_reduce<Cfg::D2>(dyp, 32);
-            if (ok && lane < Cfg::D2) {
-                float v = 0.f;
-#pragma unroll
-                for (int t = 0; t < Cfg::D2; ++t) v = lane == t ? dyp[t] : v;
-                dy[e * Cfg::D2 + lane] = v;
-            }
+            int di = 0;
+            const float dsum = warp_sum_transposed<Cfg::D2>(dyp, lane, &di);
+            if (ok && (lane & (32 / Cfg::D2 - 1)) == 0) dy[e * Cfg::D2 + di] = dsum;
         }
 #pragma unroll
         for (int r = 0; r < Cfg::D1; ++r)
