@@ -92,6 +92,22 @@ def tp_bytes(R, d1, d2, P, D, Nq, s):
     return fwd, bwd
 
 
+def max_over_ranks(seconds: float, device=None) -> float:
+    """The slowest rank's time (all_reduce MAX); the local time when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, seconds: float) -> float:
+    """Units processed by all ranks per second of the slowest rank (weak scaling)."""
+    return units_per_rank_step * steps * world / seconds
+
+
 # ---------------------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------------------
@@ -294,11 +310,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    elapsed = t0.elapsed_time(t1) / 1e3
-    if world > 1:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dev)
     ksh = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     kfw = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     kbw = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
@@ -395,13 +407,9 @@ def run_ours(args):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        te = a0.elapsed_time(a1) / 1e3
-        if world > 1:
-            tt = torch.tensor([te], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
+        te = max_over_ranks(a0.elapsed_time(a1) / 1e3, dev)
         e3.check_device_status()
-        e2e = {"value": E * ke * world / te, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        e2e = {"value": whole_job_rate(E, ke, world, te), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": ke, "ms_per_step": te / ke * 1e3,
                "includes": "pinned H2D of vec, rowptr, sender, x, w, dm; SH; graph_prepare; conv fwd; conv bwd; D2H of m, dx, dy, dw"}
         del h_w, o_dw
@@ -424,7 +432,8 @@ def run_ours(args):
                "sample": f"{n_recv} random receivers ({e_cnt} edges): oracle conv fwd + dy/dw of those edges + dx of {n_recv} senders, f64, {secs:.1f} s"}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": E * args.steps * world / elapsed, "unit": UNIT, "n_gpus": world,
+        line = {"metric": METRIC, "value": whole_job_rate(E, args.steps, world, elapsed), "unit": UNIT,
+                "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if bf16 else "f32", "data": "synthetic", "config": workload_config(w, g, args),
