@@ -224,6 +224,89 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _median(xs):
+    return float(statistics.median(xs))
+
+
+def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: str = "cell"):
+    """Per-kernel device times of SH, conv forward and conv backward on one conv workload."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import STREAM_GRAD, STREAM_W, device_normal
+    from synth import workloads as W
+    s = 2 if dt == torch.bfloat16 else 4
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    g = W.make_graph(wl, order=order)
+    N, E, Nq, P, D = g.n_nodes, g.n_edges, wl.mul, t.n_paths, t.D
+    scale = N / E
+    x_np, _ = W.make_conv(wl, g, P, edge_ids=np.zeros(0, np.int64))
+    xd = torch.from_numpy(x_np).to(dev).to(dt)
+    vec = torch.from_numpy(g.vec.astype(np.float32)).to(dev)
+    rp = torch.from_numpy(g.rowptr).to(dev)
+    sd = torch.from_numpy(g.sender).to(dev)
+    wd = device_normal((E, P, Nq), (wl.wid, STREAM_W), W.weight_scale(wl, P), device=dev, dtype=dt)
+    dmd = device_normal((N, D, Nq), (wl.wid, STREAM_GRAD), device=dev, dtype=dt)
+    y = torch.empty((E, t.d2), device=dev, dtype=dt)
+    f32 = dict(dtype=torch.float32)
+    m = torch.empty((N, D, Nq), device=dev, **f32)
+    dx, dy, dw = torch.empty_like(xd, **f32), torch.empty_like(y, **f32), torch.empty_like(wd, **f32)
+    csc = e3.graph_prepare(rp, sd, N)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        ev[k][0].record(stream)
+        e3.sh_forward(vec, wl.sh_lmax, out=y, stream=stream)
+        ev[k][1].record(stream)
+        e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream)
+        ev[k][2].record(stream)
+        e3.conv_backward(t, csc, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream)
+        ev[k][3].record(stream)
+    torch.cuda.synchronize()
+    e3.check_device_status()
+    tsh = _median([e[0].elapsed_time(e[1]) for e in ev[2:]]) / 1e3
+    tf = _median([e[1].elapsed_time(e[2]) for e in ev[2:]]) / 1e3
+    tb = _median([e[2].elapsed_time(e[3]) for e in ev[2:]]) / 1e3
+    bf, bb = conv_bytes(N, E, t.d1, t.d2, P, D, Nq, s)
+    out = {"workload": wl.name, "dtype": "bf16" if s == 2 else "f32", "atoms": N, "edges": E,
+           "sh_ms": tsh * 1e3,
+           "fwd": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bf / tf / 1e9, "frac": bf / tf / 1e9 / hbm_peak},
+           "bwd": {"ms": tb * 1e3, "edges_per_s": E / tb, "alg_GBps": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak},
+           "fwd_bwd_edges_per_s": E / (tf + tb + tsh)}
+    del xd, wd, dmd, y, m, dx, dy, dw
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_tp_workload(wl, dev, stream, reps: int, hbm_peak: float):
+    """Per-kernel device times of TP forward and backward on a row workload (fp32)."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import workloads as W
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    u, x, ww = W.make_tp(wl, t.n_paths)
+    R = x.shape[0]
+    xd, wd = torch.from_numpy(x).to(dev), torch.from_numpy(ww).to(dev)
+    y = e3.sh_forward(torch.from_numpy(u.astype(np.float32)).to(dev), wl.sh_lmax)
+    dz = torch.from_numpy(W.make_grad(wl, R, t.D)).to(dev)
+    z = torch.empty((R, t.D, wl.mul), device=dev)
+    gx, gy, gw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        ev[k][0].record(stream)
+        e3.tp_forward(t, xd, y, wd, out=z, stream=stream)
+        ev[k][1].record(stream)
+        e3.tp_backward(t, xd, y, wd, dz, out=(gx, gy, gw), stream=stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    tf = _median([e[0].elapsed_time(e[1]) for e in ev[2:]]) / 1e3
+    tb = _median([e[1].elapsed_time(e[2]) for e in ev[2:]]) / 1e3
+    btf, btb = tp_bytes(R, t.d1, t.d2, t.n_paths, t.D, wl.mul, 4)
+    return {"workload": wl.name, "dtype": "f32", "rows": R,
+            "fwd": {"ms": tf * 1e3, "rows_per_s": R / tf, "alg_GBps": btf / tf / 1e9, "frac": btf / tf / 1e9 / hbm_peak},
+            "bwd": {"ms": tb * 1e3, "rows_per_s": R / tb, "alg_GBps": btb / tb / 1e9, "frac": btb / tb / 1e9 / hbm_peak}}
+
+
 def workload_config(w, g, args):
     return {"workload": f"{w.name} ({args.dtype})", "atoms": g.n_nodes, "edges": g.n_edges,
             "atom_order": args.order, "parallelism": "replicas" if args.gpus > 1 else "single",
@@ -413,16 +496,26 @@ def run_ours(args):
                "steps": ke, "ms_per_step": te / ke * 1e3,
                "includes": "pinned H2D of vec, rowptr, sender, x, w, dm; SH; graph_prepare; conv fwd; conv bwd; D2H of m, dx, dy, dw"}
         del h_w, o_dw
+    # ---- the other workloads (kernel times only; rank 0)
+    others = None
+    if rank == 0 and not args.no_workloads:
+        del wd, dmd, dx, dy, dw, xd, y, m
+        torch.cuda.empty_cache()
+        others = [time_tp_workload(W.WORKLOADS[1], dev, stream, 20, hbm_peak),
+                  time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak),
+                  time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak),
+                  time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak)]
+
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         from synth import STREAM_GRAD as SG
         ot = oracle.table(w.blocks, w.sh_lmax, w.out_lmax)
-        wfetch = lambda ids: wd[torch.from_numpy(np.asarray(ids, np.int64)).to(dev)].float().cpu().numpy().astype(np.float64)
-        xo = xd.float().cpu().numpy().astype(np.float64)
-        yo = oracle.sh(g.vec.astype(np.float32).astype(np.float64), w.sh_lmax)
-        dmo = dmd.float().cpu().numpy().astype(np.float64)
+        P = t.n_paths
+        wfetch = lambda ids: W.make_conv(w, g, P, edge_ids=np.asarray(ids, np.int64))[1].astype(np.float64)
+        xo, yo = cpu_inputs(w, g, ot)
+        dmo = W.make_grad(w, N, t.D).astype(np.float64)
         n_recv = 8
         e_cnt, secs = oracle_conv_sample(w, g, ot, xo, yo, wfetch, dmo, scale, n_recv, seed=5)
         # grow the sample to about 10 s of CPU work
@@ -438,7 +531,7 @@ def run_ours(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if bf16 else "f32", "data": "synthetic", "config": workload_config(w, g, args),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps,
-                "clocks": clk, "rows": rows, "tp": tp}
+                "clocks": clk, "rows": rows, "tp": tp, "workloads": others}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -459,6 +552,7 @@ def main():
     ap.add_argument("--no-tp", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload kernel timings")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

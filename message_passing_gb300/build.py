@@ -58,7 +58,9 @@ def units() -> list[tuple[str, str, list[str]]]:
     u = [(os.path.join(CSRC, s), os.path.join(OBJDIR, s.replace(".cu", ".o")), [])
          for s in ("api.cu", "sh.cu", "graph.cu")]
     for i in config_ids():
-        u.append((os.path.join(CSRC, "instances.cu"), os.path.join(OBJDIR, f"cfg{i}.o"), [f"-DE3GB_CFG={i}"]))
+        for part in (0, 1):   # forward half, backward half
+            u.append((os.path.join(CSRC, "instances.cu"), os.path.join(OBJDIR, f"cfg{i}_{part}.o"),
+                      [f"-DE3GB_CFG={i}", f"-DE3GB_PART={part}"]))
     return u
 
 

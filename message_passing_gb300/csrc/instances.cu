@@ -1,11 +1,14 @@
-// One irreps configuration's kernels and launchers; compiled once per entry of configs.def
-// with -DE3GB_CFG=<id>, each unit exporting e3gb::ops_<id>().
+// One irreps configuration's kernels and launchers; compiled twice per entry of configs.def,
+// with -DE3GB_CFG=<id> -DE3GB_PART=0 (forward kernels and the ops table e3gb::ops_<id>())
+// and -DE3GB_PART=1 (backward kernels), so that the two halves compile in parallel.
 #include "conv_pipe.cuh"
 #include "kernels.cuh"
 
-#ifndef E3GB_CFG
-#error "compile with -DE3GB_CFG=<config id>"
+#if !defined(E3GB_CFG) || !defined(E3GB_PART)
+#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1>"
 #endif
+#define E3GB_CAT2(a, b) a##b
+#define E3GB_CAT(a, b) E3GB_CAT2(a, b)
 
 namespace e3gb {
 
@@ -27,25 +30,47 @@ struct Pick;
 #include "configs.def"
 #undef E3GB_CONFIG
 
-namespace {
+namespace E3GB_CAT(cfg, E3GB_CFG) {
 using Cfg = typename Pick<E3GB_CFG>::type;
 constexpr int kBlock = 256;
 
-int rows_per_block(int Nq) { return (kBlock / 32) * (32 / (Nq / kVec)); }
+// channels per lane of the plain kernels: 4 for wide rows, 1 for narrow ones (keeps the
+// accumulators of all output rows in registers without spilling)
+constexpr int vec_for(int Nq) { return Nq >= 64 ? 4 : 1; }
+static int rows_per_block(int Nq) { return (kBlock / 32) * (32 / (Nq / vec_for(Nq))); }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <class T>
+cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* w, void* z, cudaStream_t s);
+template <class T>
+cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* w, const void* dz, void* dx,
+                   void* dy, void* dw, cudaStream_t s);
+template <class T>
+cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                     const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s);
+template <class T>
+cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
+                     const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
+                     void* dw, unsigned* err, cudaStream_t s);
+
+#if E3GB_PART == 0
+template <class T>
 cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* w, void* z, cudaStream_t s) {
-    auto k = tp_forward_kernel<Cfg, T>;
+    auto k = vec_for(Nq) == 4 ? tp_forward_kernel<Cfg, T, 4> : tp_forward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (float*)z);
     return cudaGetLastError();
 }
 
+#endif  // part 0
+
+#if E3GB_PART == 1
 template <class T>
 cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* w, const void* dz, void* dx,
                    void* dy, void* dw, cudaStream_t s) {
-    auto k = tp_backward_kernel<Cfg, T>;
+    auto k = vec_for(Nq) == 4 ? tp_backward_kernel<Cfg, T, 4> : tp_backward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (const T*)dz, (float*)dx,
@@ -53,8 +78,9 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
     return cudaGetLastError();
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+#endif  // part 1
 
+#if E3GB_PART == 0
 template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
                      const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s) {
@@ -72,7 +98,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
             return cudaGetLastError();
         }
     }
-    auto k = conv_forward_kernel<Cfg, T>;
+    auto k = vec_for(Nq) == 4 ? conv_forward_kernel<Cfg, T, 4> : conv_forward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
@@ -80,6 +106,9 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
     return cudaGetLastError();
 }
 
+#endif  // part 0
+
+#if E3GB_PART == 1
 template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
@@ -98,7 +127,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
             return cudaGetLastError();
         }
     }
-    auto k = conv_backward_kernel<Cfg, T>;
+    auto k = vec_for(Nq) == 4 ? conv_backward_kernel<Cfg, T, 4> : conv_backward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
@@ -106,6 +135,22 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
     return cudaGetLastError();
 }
 
+template cudaError_t tp_bwd<float>(int64_t, int, const void*, const void*, const void*, const void*, void*, void*,
+                                    void*, cudaStream_t);
+template cudaError_t tp_bwd<__nv_bfloat16>(int64_t, int, const void*, const void*, const void*, const void*, void*,
+                                            void*, void*, cudaStream_t);
+template cudaError_t conv_bwd<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                      const void*, const void*, const void*, const void*, float, void*, void*, void*,
+                                      unsigned*, cudaStream_t);
+template cudaError_t conv_bwd<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                              const void*, const void*, const void*, const void*, float, void*, void*,
+                                              void*, unsigned*, cudaStream_t);
+#endif  // part 1
+}  // namespace cfg<id>
+
+#if E3GB_PART == 0
+namespace {
+using namespace E3GB_CAT(cfg, E3GB_CFG);
 const ConfigOps kOps = {
     Cfg::xcode, Cfg::L2, Cfg::L3, Cfg::per_path ? 1 : 0,
     Cfg::NP, Cfg::D1, Cfg::D2, Cfg::D, Cfg::NOUT, Cfg::NR,
@@ -117,8 +162,7 @@ const ConfigOps kOps = {
 };
 }  // namespace
 
-#define E3GB_CAT2(a, b) a##b
-#define E3GB_CAT(a, b) E3GB_CAT2(a, b)
 const ConfigOps* E3GB_CAT(ops_, E3GB_CFG)() { return &kOps; }
+#endif
 
 }  // namespace e3gb

@@ -85,6 +85,22 @@ struct IO<__nv_bfloat16> {
     }
 };
 
+// V consecutive channels (V = 1 or 4) of one row
+template <class T, int V>
+__device__ __forceinline__ void loadv(const T* __restrict__ p, float (&o)[V]) {
+    if constexpr (V == 4) IO<T>::load4(p, o);
+    else
+#pragma unroll
+        for (int c = 0; c < V; ++c) o[c] = IO<T>::load1(p + c);
+}
+template <int V>
+__device__ __forceinline__ void storev(float* __restrict__ p, const float (&o)[V]) {
+    if constexpr (V == 4) IO<float>::store4(p, o);
+    else
+#pragma unroll
+        for (int c = 0; c < V; ++c) p[c] = o[c];
+}
+
 // ------------------------------------------------------------------------------------------
 // per-configuration constant helpers
 // ------------------------------------------------------------------------------------------
@@ -129,42 +145,42 @@ __device__ __forceinline__ void build_A(const float (&yv)[Cfg::D2], float (&A)[O
 }
 
 // acc[m3][c] += w[c] * sum_m1 A[m3][m1] x[xoff + m1][c] for path P.
-template <class Cfg, int P, int NROWS>
+template <class Cfg, int P, int NROWS, int V>
 __device__ __forceinline__ void apply_path(const float (&A)[Off<Cfg>::a[P + 1] - Off<Cfg>::a[P]],
-                                           const float (&xv)[Cfg::D1][kVec], const float (&wv)[kVec],
-                                           float (&acc)[NROWS][kVec], int row0) {
+                                           const float (&xv)[Cfg::D1][V], const float (&wv)[V],
+                                           float (&acc)[NROWS][V], int row0) {
     constexpr PathInfo pi = Cfg::table.paths[P];
     constexpr int a0 = Off<Cfg>::a[P];
     constexpr int na = Off<Cfg>::a[P + 1] - a0;
     constexpr int n1 = 2 * pi.l1 + 1, n3 = 2 * pi.l3 + 1;
     if constexpr (n1 <= n3) {
-        float xw[n1][kVec];
+        float xw[n1][V];
 #pragma unroll
         for (int m = 0; m < n1; ++m)
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) xw[m][c] = wv[c] * xv[pi.xoff + m][c];
+            for (int c = 0; c < V; ++c) xw[m][c] = wv[c] * xv[pi.xoff + m][c];
         sfor<na>([&](auto k) {
             constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
 #pragma unroll
-            for (int c = 0; c < kVec; ++c)
+            for (int c = 0; c < V; ++c)
                 acc[row0 + e.m3][c] = fmaf(A[decltype(k)::value], xw[e.m1][c], acc[row0 + e.m3][c]);
         });
     } else {
-        float t[n3][kVec];
+        float t[n3][V];
 #pragma unroll
         for (int m = 0; m < n3; ++m)
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) t[m][c] = 0.f;
+            for (int c = 0; c < V; ++c) t[m][c] = 0.f;
         sfor<na>([&](auto k) {
             constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
 #pragma unroll
-            for (int c = 0; c < kVec; ++c)
+            for (int c = 0; c < V; ++c)
                 t[e.m3][c] = fmaf(A[decltype(k)::value], xv[pi.xoff + e.m1][c], t[e.m3][c]);
         });
 #pragma unroll
         for (int m = 0; m < n3; ++m)
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) acc[row0 + m][c] = fmaf(wv[c], t[m][c], acc[row0 + m][c]);
+            for (int c = 0; c < V; ++c) acc[row0 + m][c] = fmaf(wv[c], t[m][c], acc[row0 + m][c]);
     }
 }
 
@@ -175,9 +191,10 @@ struct Lanes {
     int per_warp; // rows per warp
 };
 
+template <int V>
 __device__ __forceinline__ Lanes lanes_for(int Nq) {
     Lanes L;
-    L.G = Nq / kVec;
+    L.G = Nq / V;
     const int lane = threadIdx.x & 31;
     L.grp = lane / L.G;
     L.gl = lane % L.G;
@@ -188,42 +205,42 @@ __device__ __forceinline__ Lanes lanes_for(int Nq) {
 // ------------------------------------------------------------------------------------------
 // TP forward on rows: output block by output block, so only one block's accumulators live.
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T>
+template <class Cfg, class T, int V>
 __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, const T* __restrict__ x,
                                                          const T* __restrict__ y, const T* __restrict__ w,
                                                          float* __restrict__ z) {
-    const Lanes L = lanes_for(Nq);
+    const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int c0 = L.gl * kVec;
+    const int c0 = L.gl * V;
     for (int64_t r = warp * L.per_warp + L.grp; r < R; r += nwarp * L.per_warp) {
         float yv[Cfg::D2];
 #pragma unroll
         for (int i = 0; i < Cfg::D2; ++i) yv[i] = IO<T>::load1(y + r * Cfg::D2 + i);
-        float xv[Cfg::D1][kVec];
+        float xv[Cfg::D1][V];
 #pragma unroll
-        for (int i = 0; i < Cfg::D1; ++i) IO<T>::load4(x + (r * Cfg::D1 + i) * Nq + c0, xv[i]);
+        for (int i = 0; i < Cfg::D1; ++i) loadv<T, V>(x + (r * Cfg::D1 + i) * Nq + c0, xv[i]);
         sfor<Cfg::NOUT>([&](auto jj) {
             constexpr int j = decltype(jj)::value;
             constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
-            float acc[nrow][kVec];
+            float acc[nrow][V];
 #pragma unroll
             for (int m = 0; m < nrow; ++m)
 #pragma unroll
-                for (int c = 0; c < kVec; ++c) acc[m][c] = 0.f;
+                for (int c = 0; c < V; ++c) acc[m][c] = 0.f;
             sfor<Cfg::NP>([&](auto pp) {
                 constexpr int p = decltype(pp)::value;
                 if constexpr (Cfg::table.paths[p].out_block == j) {
                     float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
                     build_A<Cfg, p>(yv, A);
-                    float wv[kVec];
-                    IO<T>::load4(w + (r * Cfg::NP + p) * Nq + c0, wv);
-                    apply_path<Cfg, p, nrow>(A, xv, wv, acc, 0);
+                    float wv[V];
+                    loadv<T, V>(w + (r * Cfg::NP + p) * Nq + c0, wv);
+                    apply_path<Cfg, p, nrow, V>(A, xv, wv, acc, 0);
                 }
             });
             constexpr int zo = Off<Cfg>::z[j];
 #pragma unroll
-            for (int m = 0; m < nrow; ++m) IO<float>::store4(z + (r * Cfg::D + zo + m) * Nq + c0, acc[m]);
+            for (int m = 0; m < nrow; ++m) storev<V>(z + (r * Cfg::D + zo + m) * Nq + c0, acc[m]);
         });
     }
 }
@@ -237,21 +254,21 @@ __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, cons
 //   dx[m1][q] += w[p][q] g_p[m1][q]
 //   dy[m2]    += sum_{records (m1,m2,m3,c)} c * sum_q x[m1][q] w[p][q] g[m3][q]
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T>
-__device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], const float (&yv)[Cfg::D2],
+template <class Cfg, class T, int V>
+__device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][V], const float (&yv)[Cfg::D2],
                                               const T* __restrict__ w_e, const T* __restrict__ g_row,
                                               float gscale, float* __restrict__ dw_e, int Nq, int c0,
-                                              float (&dxa)[Cfg::D1][kVec], float (&dyp)[Cfg::D2]) {
+                                              float (&dxa)[Cfg::D1][V], float (&dyp)[Cfg::D2]) {
     sfor<Cfg::NOUT>([&](auto jj) {
         constexpr int j = decltype(jj)::value;
         constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
         constexpr int zo = Off<Cfg>::z[j];
-        float g[nrow][kVec];
+        float g[nrow][V];
 #pragma unroll
         for (int m = 0; m < nrow; ++m) {
-            IO<T>::load4(g_row + (zo + m) * Nq + c0, g[m]);
+            loadv<T, V>(g_row + (zo + m) * Nq + c0, g[m]);
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) g[m][c] *= gscale;
+            for (int c = 0; c < V; ++c) g[m][c] *= gscale;
         }
         sfor<Cfg::NP>([&](auto pp) {
             constexpr int p = decltype(pp)::value;
@@ -262,14 +279,14 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], 
                 constexpr int n1 = 2 * pi.l1 + 1;
                 float A[na];
                 build_A<Cfg, p>(yv, A);
-                float wv[kVec];
-                IO<T>::load4(w_e + p * Nq + c0, wv);
-                float gp[n1][kVec];
-                float xw[n1][kVec];
+                float wv[V];
+                loadv<T, V>(w_e + p * Nq + c0, wv);
+                float gp[n1][V];
+                float xw[n1][V];
 #pragma unroll
                 for (int m = 0; m < n1; ++m)
 #pragma unroll
-                    for (int c = 0; c < kVec; ++c) {
+                    for (int c = 0; c < V; ++c) {
                         gp[m][c] = 0.f;
                         xw[m][c] = xv[pi.xoff + m][c] * wv[c];
                     }
@@ -277,7 +294,7 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], 
                     constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
                     float s = 0.f;
 #pragma unroll
-                    for (int c = 0; c < kVec; ++c) {
+                    for (int c = 0; c < V; ++c) {
                         gp[e.m1][c] = fmaf(A[decltype(k)::value], g[e.m3][c], gp[e.m1][c]);
                         s = fmaf(xw[e.m1][c], g[e.m3][c], s);
                     }
@@ -286,9 +303,9 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], 
                         dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
                     });
                 });
-                float dwv[kVec];
+                float dwv[V];
 #pragma unroll
-                for (int c = 0; c < kVec; ++c) {
+                for (int c = 0; c < V; ++c) {
                     float s = 0.f;
 #pragma unroll
                     for (int m = 0; m < n1; ++m) {
@@ -297,7 +314,7 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][kVec], 
                     }
                     dwv[c] = s;
                 }
-                IO<float>::store4(dw_e + p * Nq + c0, dwv);
+                storev<V>(dw_e + p * Nq + c0, dwv);
             }
         });
     });
@@ -312,22 +329,22 @@ __device__ __forceinline__ void group_reduce(float (&v)[N], int G) {
     }
 }
 
-template <class Cfg, class T>
+template <class Cfg, class T, int V>
 __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, const T* __restrict__ x,
                                                           const T* __restrict__ y, const T* __restrict__ w,
                                                           const T* __restrict__ dz, float* __restrict__ dx,
                                                           float* __restrict__ dy, float* __restrict__ dw) {
-    const Lanes L = lanes_for(Nq);
+    const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int c0 = L.gl * kVec;
+    const int c0 = L.gl * V;
     // every lane of the warp runs the same trip count so the group shuffles stay converged
     const int64_t iters = (R + nwarp * L.per_warp - 1) / (nwarp * L.per_warp);
     for (int64_t it = 0; it < iters; ++it) {
         const int64_t r = (it * nwarp + warp) * L.per_warp + L.grp;
         const bool live = r < R;
         const int64_t rr = live ? r : 0;
-        float yv[Cfg::D2], xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec], dyp[Cfg::D2];
+        float yv[Cfg::D2], xv[Cfg::D1][V], dxa[Cfg::D1][V], dyp[Cfg::D2];
 #pragma unroll
         for (int i = 0; i < Cfg::D2; ++i) {
             yv[i] = live ? IO<T>::load1(y + rr * Cfg::D2 + i) : 0.f;
@@ -335,20 +352,20 @@ __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, con
         }
 #pragma unroll
         for (int i = 0; i < Cfg::D1; ++i) {
-            if (live) IO<T>::load4(x + (rr * Cfg::D1 + i) * Nq + c0, xv[i]);
+            if (live) loadv<T, V>(x + (rr * Cfg::D1 + i) * Nq + c0, xv[i]);
             else
 #pragma unroll
-                for (int c = 0; c < kVec; ++c) xv[i][c] = 0.f;
+                for (int c = 0; c < V; ++c) xv[i][c] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) dxa[i][c] = 0.f;
+            for (int c = 0; c < V; ++c) dxa[i][c] = 0.f;
         }
         if (live)
-            backward_body<Cfg, T>(xv, yv, w + rr * Cfg::NP * Nq, dz + rr * Cfg::D * Nq, 1.f,
+            backward_body<Cfg, T, V>(xv, yv, w + rr * Cfg::NP * Nq, dz + rr * Cfg::D * Nq, 1.f,
                                   dw + rr * Cfg::NP * Nq, Nq, c0, dxa, dyp);
         group_reduce<Cfg::D2>(dyp, L.G);
         if (live) {
 #pragma unroll
-            for (int i = 0; i < Cfg::D1; ++i) IO<float>::store4(dx + (rr * Cfg::D1 + i) * Nq + c0, dxa[i]);
+            for (int i = 0; i < Cfg::D1; ++i) storev<V>(dx + (rr * Cfg::D1 + i) * Nq + c0, dxa[i]);
             if (L.gl == 0)
 #pragma unroll
                 for (int i = 0; i < Cfg::D2; ++i) dy[rr * Cfg::D2 + i] = dyp[i];
@@ -360,23 +377,23 @@ __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, con
 // Convolution forward: one row group per receiver, all D output rows in registers, edges
 // of the receiver in CSR order (Alg. 2 receiver-stationary aggregation).
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T>
+template <class Cfg, class T, int V>
 __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E, int Nq,
                                                            const int32_t* __restrict__ rowptr,
                                                            const int32_t* __restrict__ sender,
                                                            const T* __restrict__ x, const T* __restrict__ y,
                                                            const T* __restrict__ w, float scale,
                                                            float* __restrict__ m, unsigned* __restrict__ err) {
-    const Lanes L = lanes_for(Nq);
+    const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int c0 = L.gl * kVec;
+    const int c0 = L.gl * V;
     for (int64_t b = warp * L.per_warp + L.grp; b < N; b += nwarp * L.per_warp) {
-        float acc[Cfg::D][kVec];
+        float acc[Cfg::D][V];
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i)
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) acc[i][c] = 0.f;
+            for (int c = 0; c < V; ++c) acc[i][c] = 0.f;
         int64_t e0 = __ldg(rowptr + b), e1 = __ldg(rowptr + b + 1);
         if (e0 < 0 || e1 < e0 || e1 > E) {
             if (L.gl == 0) atomicOr(err, kErrRowptr);
@@ -391,23 +408,23 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
             float yv[Cfg::D2];
 #pragma unroll
             for (int i = 0; i < Cfg::D2; ++i) yv[i] = IO<T>::load1(y + e * Cfg::D2 + i);
-            float xv[Cfg::D1][kVec];
+            float xv[Cfg::D1][V];
 #pragma unroll
-            for (int i = 0; i < Cfg::D1; ++i) IO<T>::load4(x + (a * Cfg::D1 + i) * Nq + c0, xv[i]);
+            for (int i = 0; i < Cfg::D1; ++i) loadv<T, V>(x + (a * Cfg::D1 + i) * Nq + c0, xv[i]);
             sfor<Cfg::NP>([&](auto pp) {
                 constexpr int p = decltype(pp)::value;
                 float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
                 build_A<Cfg, p>(yv, A);
-                float wv[kVec];
-                IO<T>::load4(w + (e * Cfg::NP + p) * Nq + c0, wv);
-                apply_path<Cfg, p, Cfg::D>(A, xv, wv, acc, Cfg::table.paths[p].zoff);
+                float wv[V];
+                loadv<T, V>(w + (e * Cfg::NP + p) * Nq + c0, wv);
+                apply_path<Cfg, p, Cfg::D, V>(A, xv, wv, acc, Cfg::table.paths[p].zoff);
             });
         }
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i) {
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) acc[i][c] *= scale;
-            IO<float>::store4(m + (b * Cfg::D + i) * Nq + c0, acc[i]);
+            for (int c = 0; c < V; ++c) acc[i][c] *= scale;
+            storev<V>(m + (b * Cfg::D + i) * Nq + c0, acc[i]);
         }
     }
 }
@@ -418,30 +435,30 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
 // edges of a (csc_ptr / csc_edge / csc_recv), gathering dm of each receiver. dw and dy are
 // edge-local and written once per edge.
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T>
+template <class Cfg, class T, int V>
 __global__ void __launch_bounds__(256) conv_backward_kernel(
     int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
     const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y,
     const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
     float* __restrict__ dy, float* __restrict__ dw, unsigned* __restrict__ err) {
-    const Lanes L = lanes_for(Nq);
+    const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int c0 = L.gl * kVec;
+    const int c0 = L.gl * V;
     const int64_t iters = (N + nwarp * L.per_warp - 1) / (nwarp * L.per_warp);
     for (int64_t it = 0; it < iters; ++it) {
         const int64_t a = (it * nwarp + warp) * L.per_warp + L.grp;
         const bool live = a < N;
         const int64_t aa = live ? a : 0;
-        float xv[Cfg::D1][kVec], dxa[Cfg::D1][kVec];
+        float xv[Cfg::D1][V], dxa[Cfg::D1][V];
 #pragma unroll
         for (int i = 0; i < Cfg::D1; ++i) {
-            if (live) IO<T>::load4(x + (aa * Cfg::D1 + i) * Nq + c0, xv[i]);
+            if (live) loadv<T, V>(x + (aa * Cfg::D1 + i) * Nq + c0, xv[i]);
             else
 #pragma unroll
-                for (int c = 0; c < kVec; ++c) xv[i][c] = 0.f;
+                for (int c = 0; c < V; ++c) xv[i][c] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) dxa[i][c] = 0.f;
+            for (int c = 0; c < V; ++c) dxa[i][c] = 0.f;
         }
         int64_t k0 = 0, k1 = 0;
         if (live) {
@@ -476,7 +493,7 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
                 float yv[Cfg::D2];
 #pragma unroll
                 for (int t = 0; t < Cfg::D2; ++t) yv[t] = IO<T>::load1(y + e * Cfg::D2 + t);
-                backward_body<Cfg, T>(xv, yv, w + e * Cfg::NP * Nq, dm + b * Cfg::D * Nq, scale,
+                backward_body<Cfg, T, V>(xv, yv, w + e * Cfg::NP * Nq, dm + b * Cfg::D * Nq, scale,
                                       dw + e * Cfg::NP * Nq, Nq, c0, dxa, dyp);
             }
             group_reduce<Cfg::D2>(dyp, L.G);
@@ -486,7 +503,7 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
         }
         if (live)
 #pragma unroll
-            for (int i = 0; i < Cfg::D1; ++i) IO<float>::store4(dx + (aa * Cfg::D1 + i) * Nq + c0, dxa[i]);
+            for (int i = 0; i < Cfg::D1; ++i) storev<V>(dx + (aa * Cfg::D1 + i) * Nq + c0, dxa[i]);
     }
 }
 
