@@ -93,7 +93,7 @@ struct PipePlan {
         return o;
     }();
     // forward: w rows in NWC chunks of PPC paths
-    static constexpr int PPC = 6;
+    static constexpr int PPC = 8;   // measured: 4 / 6 / 8 / 12 / 24 paths per chunk -> 8 fastest
     static constexpr int NWC = (Cfg::NP + PPC - 1) / PPC;
     // backward: the paths of each output block, in path order
     static constexpr std::array<int, Cfg::NOUT + 1> bpos = [] {   // offsets into bpath
@@ -154,18 +154,19 @@ constexpr RecipeTable<Cfg> make_recipes() {
 template <class Cfg, bool FWD>
 __device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg, FWD>();
 
-// A entries of one edge, built by the 32 lanes of a warp from y in shared memory. Each
-// entry is stored twice, (A, A), so that a 16-byte load yields two ready operand pairs for
-// the paired (f32x2) multiply-adds of the channel loops.
+// A entries of one edge, built by the 32 lanes of a warp from y in shared memory (the
+// buffer is addressed as floats; the float2 type only gives it 8-byte units). The channel
+// loops read four entries per 16-byte load and broadcast each into an (A, A) operand pair
+// of the paired (f32x2) multiply-adds.
 template <class Cfg, bool FWD, class T>
 __device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float2* __restrict__ sA, int lane) {
-#pragma unroll 2
+#pragma unroll   // fully unrolled: the recipe loads of all entries issue together (measured)
     for (int i = lane; i < Cfg::NA; i += 32) {
         const Recipe r = kRecipes<Cfg, FWD>.r[i];
         const int i0 = r.idx & 0xff, i1 = (r.idx >> 8) & 0xff;
         float v = r.c0 * float(sy[i0]);
         if ((r.idx >> 16) > 1) v = fmaf(r.c1, float(sy[i1]), v);
-        sA[r.pos] = make_float2(v, v);
+        reinterpret_cast<float*>(sA)[r.pos] = v;
     }
 }
 
@@ -199,12 +200,13 @@ __device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2
         Q2 xw[n1];
 #pragma unroll
         for (int m = 0; m < n1; ++m) xw[m] = q2_mul(xv[pi.xoff + m], wv);
-        sfor<(na + 1) / 2>([&](auto qq) {
+        sfor<(na + 3) / 4>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
-            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
-            sfor<2>([&](auto cc) {
-                constexpr int kk = 2 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sA) + base + 4 * q);
+            const float2 av[4] = {make_float2(t4.x, t4.x), make_float2(t4.y, t4.y), make_float2(t4.z, t4.z),
+                                  make_float2(t4.w, t4.w)};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[PipePlan<Cfg>::fwd_order[a0 + kk]];
                     acc[Z + e.m3] = q2_fma(av[decltype(cc)::value], xw[e.m1], acc[Z + e.m3]);
@@ -215,12 +217,13 @@ __device__ __forceinline__ void fwd_path(const float2* __restrict__ sA, const Q2
         Q2 t[n3];
 #pragma unroll
         for (int m = 0; m < n3; ++m) t[m] = q2_zero();
-        sfor<(na + 1) / 2>([&](auto qq) {
+        sfor<(na + 3) / 4>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
-            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
-            sfor<2>([&](auto cc) {
-                constexpr int kk = 2 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sA) + base + 4 * q);
+            const float2 av[4] = {make_float2(t4.x, t4.x), make_float2(t4.y, t4.y), make_float2(t4.z, t4.z),
+                                  make_float2(t4.w, t4.w)};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[PipePlan<Cfg>::fwd_order[a0 + kk]];
                     t[e.m3] = q2_fma(av[decltype(cc)::value], xv[pi.xoff + e.m1], t[e.m3]);
@@ -273,7 +276,7 @@ struct FwdPipe {
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWS = Cfg::D1 > PP::PPC ? Cfg::D1 : PP::PPC;
     static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8;
+    static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
 };
 
 template <class Cfg, class T, int NSLOT, int WARPS>
@@ -398,6 +401,8 @@ struct BwdPipe {
     static constexpr int ROWS = Cfg::D1 > PP::max_block_rows ? Cfg::D1 : PP::max_block_rows;
     static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
     static constexpr int XBUF = Cfg::D1 * kPipeNq * 4;            // the sender's x rows (fp32)
+    // the A buffer is given 8 bytes per entry although it uses 4: this layout measured ~3%
+    // faster than the compact one on the 64k-atom workload
     static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8 + XBUF;
     static constexpr int NCH = Cfg::NOUT;   // items per edge (one per output block)
 };
@@ -432,12 +437,13 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
             gp[mm] = q2_zero();
             xw[mm] = q2_mul(xr[mm], wv);
         }
-        sfor<(na + 1) / 2>([&](auto qq) {
+        sfor<(na + 3) / 4>([&](auto qq) {
             constexpr int q = decltype(qq)::value;
-            const float4 t4 = *reinterpret_cast<const float4*>(sA + base + 2 * q);
-            const float2 av[2] = {make_float2(t4.x, t4.y), make_float2(t4.z, t4.w)};
-            sfor<2>([&](auto cc) {
-                constexpr int kk = 2 * q + decltype(cc)::value;
+            const float4 t4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sA) + base + 4 * q);
+            const float2 av[4] = {make_float2(t4.x, t4.x), make_float2(t4.y, t4.y), make_float2(t4.z, t4.z),
+                                  make_float2(t4.w, t4.w)};
+            sfor<4>([&](auto cc) {
+                constexpr int kk = 4 * q + decltype(cc)::value;
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
                     gp[e.m1] = q2_fma(av[decltype(cc)::value], g[e.m3], gp[e.m1]);
