@@ -77,3 +77,40 @@ def sh(vec: np.ndarray, lmax: int) -> np.ndarray:
         raise ValueError("lmax must be in 0..3")
     u = normalise(vec)
     return np.concatenate([sh_l(u, l) for l in range(lmax + 1)], axis=1)
+
+
+def _poly_grad(poly: dict, u: np.ndarray) -> np.ndarray:
+    """Gradient of a polynomial {(a,b,c): k} at the rows of u: [n, 3]."""
+    x, y, z = u[:, 0], u[:, 1], u[:, 2]
+    g = np.zeros((u.shape[0], 3))
+    for (a, b, c), k in poly.items():
+        if a:
+            g[:, 0] += k * a * x ** (a - 1) * y ** b * z ** c
+        if b:
+            g[:, 1] += k * b * x ** a * y ** (b - 1) * z ** c
+        if c:
+            g[:, 2] += k * c * x ** a * y ** b * z ** (c - 1)
+    return g
+
+
+def sh_grad(vec: np.ndarray, lmax: int, dy: np.ndarray) -> np.ndarray:
+    """dvec[n,3] = sum_{l,m} dy[n, l^2 + l + m] dY_lm(vec/|vec|)/dvec (the VJP of sh()).
+
+    Y_lm(u) is the degree-l homogeneous polynomial P_lm at u = r/|r|, so by the chain rule
+    and Euler's identity grad P . u = l P:  dY/dr = (grad P(u) - l P(u) u) / |r|.
+    Zero where |r| < 1e-12 (Y is taken constant there)."""
+    vec = np.asarray(vec, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    r = np.linalg.norm(vec, axis=1)
+    ok = r >= 1e-12
+    u = normalise(vec)
+    g = np.zeros_like(vec)
+    euler = np.zeros(vec.shape[0])
+    for l in range(lmax + 1):
+        for i, poly in enumerate(POLY[l]):
+            d = dy[:, l * l + i]
+            g += d[:, None] * _poly_grad(poly, u)
+            euler += d * l * sh_l(u, l)[:, i]
+    out = np.zeros_like(vec)
+    out[ok] = (g[ok] - euler[ok, None] * u[ok]) / r[ok, None]
+    return out

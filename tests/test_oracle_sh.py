@@ -107,3 +107,38 @@ def test_rotation_equivariance_via_lstsq():
         D = np.linalg.lstsq(A, B, rcond=None)[0].T
         np.testing.assert_allclose(A @ D.T, B, atol=1e-12)
         np.testing.assert_allclose(D @ D.T, np.eye(2 * l + 1), atol=1e-12)
+
+
+@pytest.mark.parametrize("lmax", [0, 1, 2, 3])
+def test_sh_grad_finite_differences(lmax):
+    """sh_grad is the VJP of sh: <dvec, v> = d/dt <dy, sh(r + t v)> (central differences)."""
+    from oracle.sh import sh_grad
+    rng = np.random.default_rng(30 + lmax)
+    r = rng.standard_normal((25, 3)) * rng.uniform(0.3, 3.0, (25, 1))
+    dy = rng.standard_normal((25, (lmax + 1) ** 2))
+    v = rng.standard_normal((25, 3))
+    h = 1e-6
+    fd = ((dy * sh(r + h * v, lmax)).sum(1) - (dy * sh(r - h * v, lmax)).sum(1)) / (2 * h)
+    np.testing.assert_allclose((sh_grad(r, lmax, dy) * v).sum(1), fd, rtol=1e-6, atol=1e-8)
+
+
+def test_sh_grad_radial_scaling_rotation():
+    from scipy.spatial.transform import Rotation
+    from oracle.sh import sh_grad
+    rng = np.random.default_rng(40)
+    r = rng.standard_normal((30, 3))
+    dy = rng.standard_normal((30, 16))
+    g = sh_grad(r, 3, dy)
+    # Y depends on the direction only: no radial component, 1/s under r -> s r
+    np.testing.assert_allclose((g * r).sum(1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(sh_grad(2.5 * r, 3, dy), g / 2.5, atol=1e-12)
+    # rotating r and the cotangent (by the SH representation) rotates the gradient
+    R = Rotation.random(random_state=4).as_matrix()
+    u = rng.standard_normal((200, 3))
+    dyr = np.zeros_like(dy)
+    for l in range(4):
+        D = np.linalg.lstsq(sh_l(u, l), sh_l(u @ R.T, l), rcond=None)[0].T
+        dyr[:, l * l:(l + 1) ** 2] = dy[:, l * l:(l + 1) ** 2] @ D.T
+    np.testing.assert_allclose(sh_grad(r @ R.T, 3, dyr), g @ R.T, atol=1e-11)
+    # zero vector: zero gradient
+    assert np.all(sh_grad(np.zeros((1, 3)), 3, np.ones((1, 16))) == 0.0)
