@@ -159,14 +159,15 @@ __device__ const RecipeTable<Cfg> kRecipes = make_recipes<Cfg, FWD>();
 // loops read four entries per 16-byte load and broadcast each into an (A, A) operand pair
 // of the paired (f32x2) multiply-adds.
 template <class Cfg, bool FWD, class T>
-__device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float2* __restrict__ sA, int lane) {
+__device__ __forceinline__ void build_A_warp(const T* __restrict__ sy, float2* __restrict__ sA, int lane,
+                                             float mul = 1.f) {
 #pragma unroll   // fully unrolled: the recipe loads of all entries issue together (measured)
     for (int i = lane; i < Cfg::NA; i += 32) {
         const Recipe r = kRecipes<Cfg, FWD>.r[i];
         const int i0 = r.idx & 0xff, i1 = (r.idx >> 8) & 0xff;
         float v = r.c0 * float(sy[i0]);
         if ((r.idx >> 16) > 1) v = fmaf(r.c1, float(sy[i1]), v);
-        reinterpret_cast<float*>(sA)[r.pos] = v;
+        reinterpret_cast<float*>(sA)[r.pos] = v * mul;
     }
 }
 
@@ -408,20 +409,18 @@ struct BwdPipe {
 };
 
 // the part of an edge's backward that belongs to output block J; g rows from the slot
+// (the couplings in sA already carry the convolution scale; dy is scaled by the caller)
 template <class Cfg, class T, int J>
 __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float2* __restrict__ sA,
                                           const float* __restrict__ sx, Q2 (&dxa)[Cfg::D1], float (&dyp)[Cfg::D2],
-                                          float2 sc, float* __restrict__ dw_e, int c0) {
+                                          float* __restrict__ dw_e, int c0) {
     using PP = PipePlan<Cfg>;
     constexpr int ROWB = kPipeNq * sizeof(T);
     constexpr int nrow = 2 * Cfg::table.outs[J].l + 1;
     constexpr int npb = PP::bpos[J + 1] - PP::bpos[J];
     Q2 g[nrow];
 #pragma unroll
-    for (int mm = 0; mm < nrow; ++mm) {
-        const Q2 v = lds_q2<T>(reinterpret_cast<const T*>(slot + mm * ROWB) + c0);
-        g[mm] = {__fmul2_rn(v.lo, sc), __fmul2_rn(v.hi, sc)};
-    }
+    for (int mm = 0; mm < nrow; ++mm) g[mm] = lds_q2<T>(reinterpret_cast<const T*>(slot + mm * ROWB) + c0);
     sfor<npb>([&](auto ii) {
         constexpr int p = PP::bpath[PP::bpos[J] + decltype(ii)::value];
         constexpr PathInfo pi = Cfg::table.paths[p];
@@ -566,7 +565,6 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                 dxa[r] = q2_zero();
             }
         }
-        const float2 sc = make_float2(scale, scale);
         for (int64_t k = k0; k < k1; ++k) {
             const int64_t e = __ldg(cedge + k), bb = __ldg(crecv + k);
             const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
@@ -583,15 +581,17 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                 ++item;
                 if constexpr (j == 0) {
                     __syncwarp();
-                    if (ok) build_A_warp<Cfg, false, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane);
+                    if (ok)
+                        build_A_warp<Cfg, false, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane,
+                                                    scale);
                     __syncwarp();
                 }
-                if (ok) bwd_block<Cfg, T, j>(slot, sA, sx, dxa, dyp, sc, dw_e, c0);
+                if (ok) bwd_block<Cfg, T, j>(slot, sA, sx, dxa, dyp, dw_e, c0);
                 if constexpr (j == B::NCH - 1) __syncwarp();
             });
             int di = 0;
             const float dsum = warp_sum_transposed<Cfg::D2>(dyp, lane, &di);
-            if (ok && (lane & (32 / Cfg::D2 - 1)) == 0) dy[e * Cfg::D2 + di] = dsum;
+            if (ok && (lane & (32 / Cfg::D2 - 1)) == 0) dy[e * Cfg::D2 + di] = dsum * scale;
         }
 #pragma unroll
         for (int r = 0; r < Cfg::D1; ++r)
