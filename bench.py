@@ -252,7 +252,8 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
     m = torch.empty((N, D, Nq), device=dev, **f32)
     dx, dy, dw = torch.empty_like(xd, **f32), torch.empty_like(y, **f32), torch.empty_like(wd, **f32)
     csc = e3.graph_prepare(rp, sd, N)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps + 2)]
+    dvec = torch.empty_like(vec)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps + 2)]
     for k in range(reps + 2):
         ev[k][0].record(stream)
         e3.sh_forward(vec, wl.sh_lmax, out=y, stream=stream)
@@ -261,18 +262,23 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
         ev[k][2].record(stream)
         e3.conv_backward(t, csc, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream)
         ev[k][3].record(stream)
+        e3.sh_backward(vec, dy, wl.sh_lmax, out=dvec, stream=stream)   # forces through the harmonics
+        ev[k][4].record(stream)
     torch.cuda.synchronize()
     e3.check_device_status()
     tsh = _median([e[0].elapsed_time(e[1]) for e in ev[2:]]) / 1e3
     tf = _median([e[1].elapsed_time(e[2]) for e in ev[2:]]) / 1e3
     tb = _median([e[2].elapsed_time(e[3]) for e in ev[2:]]) / 1e3
+    tshb = _median([e[3].elapsed_time(e[4]) for e in ev[2:]]) / 1e3
     bf, bb = conv_bytes(N, E, t.d1, t.d2, P, D, Nq, s)
+    bshb = E * (12 + t.d2 * 4 + 12)   # vec, dy (fp32 from the backward), dvec
     out = {"workload": wl.name, "dtype": "bf16" if s == 2 else "f32", "atoms": N, "edges": E,
            "sh_ms": tsh * 1e3,
+           "sh_backward": {"ms": tshb * 1e3, "alg_GBps": bshb / tshb / 1e9, "frac": bshb / tshb / 1e9 / hbm_peak},
            "fwd": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bf / tf / 1e9, "frac": bf / tf / 1e9 / hbm_peak},
            "bwd": {"ms": tb * 1e3, "edges_per_s": E / tb, "alg_GBps": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak},
            "fwd_bwd_edges_per_s": E / (tf + tb + tsh)}
-    del xd, wd, dmd, y, m, dx, dy, dw
+    del xd, wd, dmd, y, m, dx, dy, dw, dvec
     torch.cuda.empty_cache()
     return out
 
@@ -502,6 +508,7 @@ def run_ours(args):
         del wd, dmd, dx, dy, dw, xd, y, m
         torch.cuda.empty_cache()
         others = [time_tp_workload(W.WORKLOADS[1], dev, stream, 20, hbm_peak),
+                  time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak)]

@@ -115,6 +115,12 @@ e3gb_status e3gb_config_describe(int32_t i, int32_t *n_blocks, int32_t *l, int32
 e3gb_status e3gb_sh_forward(int32_t lmax, int64_t n, const float *vec, void *y,
                             e3gb_dtype dtype, void *stream);
 
+/* Its VJP, the gradient through the harmonics that forces need: dvec[e] = sum_{l,m}
+ * dy[e, l^2+l+m] dY_lm(vec[e]/|vec[e]|)/dvec[e] (zero where |vec| < 1e-12). vec: device fp32
+ * [n, 3]; dy: device [n, (lmax+1)^2] of dtype; dvec: device fp32 [n, 3]. */
+e3gb_status e3gb_sh_backward(int32_t lmax, int64_t n, const float *vec, const void *dy, float *dvec,
+                             e3gb_dtype dtype, void *stream);
+
 /* Tensor product on rows (Eq. 10-11): z[r] = sum_p w[r,p] * C_p(x[r], y[r]) into the
  * output block of path p. x [rows,d1,Nq], y [rows,d2], w [rows,P,Nq], z [rows,D,Nq]. */
 e3gb_status e3gb_tp_forward(const e3gb_table *t, int64_t rows, const void *x, const void *y,

@@ -25,6 +25,7 @@ PATHS_SUMMED, PATHS_SEPARATE = 0, 1
 SYMBOLS = (
     "e3gb_table_create", "e3gb_table_destroy", "e3gb_table_info", "e3gb_table_paths",
     "e3gb_table_coefficients", "e3gb_config_count", "e3gb_config_describe", "e3gb_sh_forward",
+    "e3gb_sh_backward",
     "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
     "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
@@ -65,6 +66,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_config_count": (i32, []),
         "e3gb_config_describe": (i32, [i32, P32, P32, P32, P32, P32, P32]),
         "e3gb_sh_forward": (i32, [i32, i64, vp, vp, i32, vp]),
+        "e3gb_sh_backward": (i32, [i32, i64, vp, vp, vp, i32, vp]),
         "e3gb_tp_forward": (i32, [vp, i64, vp, vp, vp, vp, i32, vp]),
         "e3gb_tp_backward": (i32, [vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp]),
         "e3gb_graph_prepare_workspace_bytes": (szt, [i64]),
@@ -200,6 +202,18 @@ def sh_forward(vec, lmax: int, out=None, dtype=None, stream=None):
     y = out if out is not None else torch.empty((vec.shape[0], (lmax + 1) ** 2), dtype=dt, device=vec.device)
     _check(load().e3gb_sh_forward(lmax, vec.shape[0], _ptr(vec), _ptr(y), _dtype(y), _stream(stream)))
     return y
+
+
+def sh_backward(vec, dy, lmax: int, out=None, stream=None):
+    """dvec[n, 3] (fp32) = VJP of sh_forward for the cotangent dy[n, (lmax+1)^2]."""
+    import torch
+    _contig(vec, dy)
+    if vec.dtype != torch.float32:
+        raise TypeError("vec must be float32")
+    dvec = out if out is not None else torch.empty((vec.shape[0], 3), dtype=torch.float32, device=vec.device)
+    _f32_out(dvec)
+    _check(load().e3gb_sh_backward(lmax, vec.shape[0], _ptr(vec), _ptr(dy), _ptr(dvec), _dtype(dy), _stream(stream)))
+    return dvec
 
 
 def tp_forward(t: Table, x, y, w, out=None, stream=None):

@@ -27,6 +27,7 @@ static const ConfigOps* (*const kRegistry[])() = {
 constexpr int kNumConfigs = int(sizeof(kRegistry) / sizeof(kRegistry[0]));
 
 cudaError_t sh_forward(int lmax, int64_t n, const float* vec, void* y, int bf16, cudaStream_t s);
+cudaError_t sh_backward(int lmax, int64_t n, const float* vec, const void* dy, float* dvec, int bf16, cudaStream_t s);
 size_t graph_workspace_bytes(int64_t N);
 cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
                           int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s);
@@ -253,6 +254,19 @@ e3gb_status e3gb_sh_forward(int32_t lmax, int64_t n, const float* vec, void* y, 
     E3GB_TRY(check_ptr(vec, "vec", 4, true));
     E3GB_TRY(check_ptr(y, "y", elt_bytes(dtype), true));
     return cuda_status(sh_forward(lmax, n, vec, y, dtype == E3GB_BF16, (cudaStream_t)stream), "sh_forward launch");
+}
+
+e3gb_status e3gb_sh_backward(int32_t lmax, int64_t n, const float* vec, const void* dy, float* dvec, e3gb_dtype dtype,
+                             void* stream) {
+    if (lmax < 0 || lmax > kLmax) return fail(E3GB_ERR_UNSUPPORTED, "lmax %d not in 0..3", lmax);
+    if (n < 0) return fail(E3GB_ERR_INVALID_ARG, "n < 0");
+    if (dtype != E3GB_F32 && dtype != E3GB_BF16) return fail(E3GB_ERR_INVALID_ARG, "unknown dtype");
+    if (n == 0) return ok();
+    E3GB_TRY(check_ptr(vec, "vec", 4, true));
+    E3GB_TRY(check_ptr(dy, "dy", elt_bytes(dtype), true));
+    E3GB_TRY(check_ptr(dvec, "dvec", 4, true));
+    return cuda_status(sh_backward(lmax, n, vec, dy, dvec, dtype == E3GB_BF16, (cudaStream_t)stream),
+                       "sh_backward launch");
 }
 
 e3gb_status e3gb_tp_forward(const e3gb_table* t, int64_t rows, const void* x, const void* y, const void* w, void* z,

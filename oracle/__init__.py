@@ -26,7 +26,7 @@ import numpy as np
 
 from .cg import cg_block
 from .paths import Table, make_table
-from .sh import sh
+from .sh import sh, sh_grad
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIBDIR = os.path.join(_HERE, "_lib")
@@ -207,5 +207,5 @@ def conv_backward_dx(t: Table, rowptr, sender, y, w, dm, scale: float, senders=N
     return dx
 
 
-__all__ = ["sh", "cg_block", "table", "tp_forward", "tp_backward", "conv_forward",
+__all__ = ["sh", "sh_grad", "cg_block", "table", "tp_forward", "tp_backward", "conv_forward",
            "conv_backward_edges", "conv_backward_dx", "build", "num_threads", "receivers_of"]

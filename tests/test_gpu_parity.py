@@ -216,3 +216,38 @@ def test_conv_irregular_graph_with_empty_receivers():
     w = W.Workload(94, "irregular", "conv", "16x0e+16x1o", 3, 3, n_atoms=0)
     g = random_graph(61, 500, (94, 0), empty_nodes=9)
     _conv_check(w, g)
+
+
+@pytest.mark.parametrize("lmax", [0, 1, 2, 3])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_sh_backward(lmax, dt):
+    """dvec = VJP of the harmonics (forces through the edge vectors)."""
+    rng = np.random.default_rng(50 + lmax)
+    n = 2051
+    vec = (rng.standard_normal((n, 3)) * rng.uniform(0.1, 6.0, (n, 1))).astype(np.float32)
+    vec[0] = 0.0
+    dy = rng.standard_normal((n, (lmax + 1) ** 2)).astype(np.float32)
+    dyd = to_dev(dy, dt)
+    dvec = e3.sh_backward(to_dev(vec), dyd, lmax)
+    torch.cuda.synchronize()
+    ref = oracle.sh_grad(vec.astype(np.float64), lmax, to_np(dyd))
+    # dvec scales as 1/|r|: compare |r| dvec (the gradient in the direction) so that the
+    # closest pairs do not set the RMS of the whole tensor
+    rn = np.linalg.norm(vec.astype(np.float64), axis=1, keepdims=True)
+    assert_close(to_np(dvec) * rn, ref * rn, TOL_F32, f"|r| dvec l<={lmax}")
+    assert np.all(to_np(dvec)[0] == 0.0)
+
+
+def test_sh_backward_conv_edges_full_size():
+    """All 2.56M edge vectors of the 64k-atom workload, 4096 sampled edges checked."""
+    w = W.WORKLOADS[4]
+    g = W.make_graph(w)
+    vec = g.vec.astype(np.float32)
+    dyd = torch.randn((g.n_edges, 16), device="cuda")
+    dvec = e3.sh_backward(to_dev(vec), dyd, 3)
+    torch.cuda.synchronize()
+    ids = sample_ids(g.n_edges, 4096, 13)
+    sel = torch.from_numpy(ids).cuda()
+    ref = oracle.sh_grad(vec[ids].astype(np.float64), 3, to_np(dyd[sel]))
+    rn = np.linalg.norm(vec[ids].astype(np.float64), axis=1, keepdims=True)
+    assert_close(to_np(dvec[sel]) * rn, ref * rn, TOL_F32, "|r| dvec")
