@@ -228,25 +228,39 @@ def _median(xs):
     return float(statistics.median(xs))
 
 
-def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: str = "cell"):
-    """Per-kernel device times of SH, conv forward and conv backward on one conv workload."""
+def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: str = "cell",
+                       pad_frac: float = 0.0):
+    """Per-kernel device times of SH, conv forward and conv backward on one conv workload.
+    pad_frac > 0: the same graph plus one padding node holding that fraction of all edge slots
+    (mostly pad -> pad, 2% pad -> real receivers, 1% real senders -> pad), with NaN inputs on
+    every padding row, run with pad_node set; rates count the real edges."""
     import torch
 
     import message_passing_gb300 as e3
+    import synth
     from synth import STREAM_GRAD, STREAM_W, device_normal
     from synth import workloads as W
     s = 2 if dt == torch.bfloat16 else 4
     t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
     g = W.make_graph(wl, order=order)
+    E_real, pad = g.n_edges, -1
+    x_np, _ = W.make_conv(wl, g, t.n_paths, edge_ids=np.zeros(0, np.int64))
+    if pad_frac > 0:
+        n_pad = int(round(E_real * pad_frac / (1 - pad_frac)))
+        n_out, n_in = n_pad // 50, n_pad // 100
+        g, pad, orig = synth.padded_graph(g, n_pad - n_out - n_in, n_out, n_in, (wl.wid, 9))
+        x_np = np.concatenate([x_np, np.full((1,) + x_np.shape[1:], np.nan, x_np.dtype)])
     N, E, Nq, P, D = g.n_nodes, g.n_edges, wl.mul, t.n_paths, t.D
     scale = N / E
-    x_np, _ = W.make_conv(wl, g, P, edge_ids=np.zeros(0, np.int64))
     xd = torch.from_numpy(x_np).to(dev).to(dt)
     vec = torch.from_numpy(g.vec.astype(np.float32)).to(dev)
     rp = torch.from_numpy(g.rowptr).to(dev)
     sd = torch.from_numpy(g.sender).to(dev)
     wd = device_normal((E, P, Nq), (wl.wid, STREAM_W), W.weight_scale(wl, P), device=dev, dtype=dt)
     dmd = device_normal((N, D, Nq), (wl.wid, STREAM_GRAD), device=dev, dtype=dt)
+    if pad >= 0:   # padding rows hold NaN: the kernels must not read them
+        wd.index_fill_(0, torch.from_numpy(np.nonzero(orig < 0)[0]).to(dev), float("nan"))
+        dmd[pad] = float("nan")
     y = torch.empty((E, t.d2), device=dev, dtype=dt)
     f32 = dict(dtype=torch.float32)
     m = torch.empty((N, D, Nq), device=dev, **f32)
@@ -258,21 +272,28 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
         ev[k][0].record(stream)
         e3.sh_forward(vec, wl.sh_lmax, out=y, stream=stream)
         ev[k][1].record(stream)
-        e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream)
+        e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream, pad_node=pad)
         ev[k][2].record(stream)
-        e3.conv_backward(t, csc, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream)
+        e3.conv_backward(t, csc, xd, y, wd, dmd, scale, out=(dx, dy, dw), stream=stream, pad_node=pad)
         ev[k][3].record(stream)
         e3.sh_backward(vec, dy, wl.sh_lmax, out=dvec, stream=stream)   # forces through the harmonics
         ev[k][4].record(stream)
     torch.cuda.synchronize()
     e3.check_device_status()
+    if pad >= 0:
+        assert bool(torch.isfinite(m).all()) and bool(torch.isfinite(dw).all()), "padding leaked into outputs"
     tsh = _median([e[0].elapsed_time(e[1]) for e in ev[2:]]) / 1e3
     tf = _median([e[1].elapsed_time(e[2]) for e in ev[2:]]) / 1e3
     tb = _median([e[2].elapsed_time(e[3]) for e in ev[2:]]) / 1e3
     tshb = _median([e[3].elapsed_time(e[4]) for e in ev[2:]]) / 1e3
-    bf, bb = conv_bytes(N, E, t.d1, t.d2, P, D, Nq, s)
+    # algorithmic bytes of the real graph; with padding the backward also writes the padding
+    # edges' zero dy, dw rows and scans the sender-major receiver ids
+    bf, bb = conv_bytes(N, E_real, t.d1, t.d2, P, D, Nq, s)
+    bb += (E - E_real) * (t.d2 + P * Nq) * 4 + (E * 4 if pad >= 0 else 0)
     bshb = E * (12 + t.d2 * 4 + 12)   # vec, dy (fp32 from the backward), dvec
-    out = {"workload": wl.name, "dtype": "bf16" if s == 2 else "f32", "atoms": N, "edges": E,
+    E = E_real
+    name = wl.name if pad < 0 else f"{wl.name} + {pad_frac:.0%} padding edge slots on one padding node"
+    out = {"workload": name, "dtype": "bf16" if s == 2 else "f32", "atoms": N, "edges": E,
            "sh_ms": tsh * 1e3,
            "sh_backward": {"ms": tshb * 1e3, "alg_GBps": bshb / tshb / 1e9, "frac": bshb / tshb / 1e9 / hbm_peak},
            "fwd": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bf / tf / 1e9, "frac": bf / tf / 1e9 / hbm_peak},
@@ -511,7 +532,8 @@ def run_ours(args):
                   time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak)]
+                  time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak),
+                  time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak, pad_frac=0.25)]
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None

@@ -173,11 +173,18 @@ e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const in
 /* Message-passing convolution (Eq. 12-13): for every receiver b,
  *   m[b] = scale * sum_{e in [rowptr[b], rowptr[b+1])} TP(x[sender[e]], y[e], w[e]),
  * accumulated in a fixed order in registers, written once (receivers without edges get 0).
- * x [n_nodes,d1,Nq], y [n_edges,d2], w [n_edges,P,Nq], m [n_nodes,D,Nq]. */
+ * x [n_nodes,d1,Nq], y [n_edges,d2], w [n_edges,P,Nq], m [n_nodes,D,Nq].
+ *
+ * Padding edges (e3j, Sec. 4 "Message passing convolution" and App. E: static-shape graphs
+ * route their unused edge slots to one padding node, and the kernels skip them): pad_node is
+ * that node's index, or -1 for none. Every edge whose receiver or sender is pad_node is a
+ * padding edge and is not read at all (its x, y, w may hold anything, NaN included); the
+ * padding receiver's whole segment is passed over, so its valency costs nothing, and
+ * m[pad_node] = 0. pad_node outside [-1, n_nodes) is E3GB_ERR_INVALID_ARG. */
 e3gb_status e3gb_conv_forward(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
                               const int32_t *rowptr, const int32_t *sender, const void *x,
-                              const void *y, const void *w, float scale, void *m,
-                              e3gb_dtype dtype, void *stream);
+                              const void *y, const void *w, float scale, int64_t pad_node,
+                              void *m, e3gb_dtype dtype, void *stream);
 
 /* Its VJP (Eq. 16) from dm [n_nodes,D,Nq]:
  *   dw[e,p] = scale * sum_m3 dm[b][blk p, m3] * (C_p(x[a], y[e]))[m3],
@@ -185,12 +192,15 @@ e3gb_status e3gb_conv_forward(const e3gb_table *t, int64_t n_nodes, int64_t n_ed
  *   dx[a]   = scale * sum over the edges of sender a of the y, w, dm couplings,
  * walking the graph in sender order (csc_* from e3gb_graph_prepare) so that dx[a] is summed
  * in registers in a fixed order: deterministic, no atomics, no workspace.
- * dx [n_nodes,d1,Nq], dy [n_edges,d2], dw [n_edges,P,Nq]. */
+ * dx [n_nodes,d1,Nq], dy [n_edges,d2], dw [n_edges,P,Nq].
+ * pad_node as in e3gb_conv_forward: padding edges are not read, their dw and dy rows are
+ * written as zeros (by a second, grid-wide launch on the same stream that scans csc_recv),
+ * and dx[pad_node] = 0. */
 e3gb_status e3gb_conv_backward(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
                                const int32_t *csc_ptr, const int32_t *csc_edge,
                                const int32_t *csc_recv, const void *x, const void *y,
-                               const void *w, const void *dm, float scale, void *dx, void *dy,
-                               void *dw, e3gb_dtype dtype, void *stream);
+                               const void *w, const void *dm, float scale, int64_t pad_node,
+                               void *dx, void *dy, void *dw, e3gb_dtype dtype, void *stream);
 
 /* Synchronise stream, read and clear the device error word of the current device.
  * E3GB_OK when clean, E3GB_ERR_DEVICE_INDEX when a kernel skipped bad indices (*flags, if

@@ -72,8 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_graph_prepare_workspace_bytes": (szt, [i64]),
         "e3gb_graph_prepare": (i32, [i64, i64, vp, vp, vp, vp, vp, vp, szt, vp]),
         "e3gb_graph_prepare_static": (i32, [i64, i64, vp, vp, vp, vp, vp, vp]),
-        "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, vp, i32, vp]),
-        "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, i32, vp]),
+        "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, i64, vp, i32, vp]),
+        "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, i64, vp, vp, vp, i32, vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
         "e3gb_last_error": (ctypes.c_char_p, []),
         "e3gb_version": (ctypes.c_char_p, []),
@@ -284,20 +284,23 @@ def graph_prepare_static(rowptr, sender, n_nodes: int, out=None, stream=None):
     return cp, ce, cr
 
 
-def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stream=None):
+def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stream=None, pad_node: int = -1):
+    """m = scale * sum over each receiver's CSR edges of TP(x[sender], y, w); edges touching
+    pad_node (>= 0) are padding and skipped."""
     import torch
     _contig(rowptr, sender, x, y, w)
     N, E = x.shape[0], sender.shape[0]
     m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=torch.float32, device=x.device)
     _f32_out(m)
     _check(load().e3gb_conv_forward(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
-                                    _ptr(y) if E else None, _ptr(w) if E else None, float(scale), _ptr(m),
+                                    _ptr(y) if E else None, _ptr(w) if E else None, float(scale), int(pad_node), _ptr(m),
                                     _dtype(x, *((y, w) if E else ())), _stream(stream)))
     return m
 
 
-def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=None):
-    """csc = graph_prepare(...) output. Returns (dx, dy, dw)."""
+def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=None, pad_node: int = -1):
+    """csc = graph_prepare(...) output. Returns (dx, dy, dw); padding edges (touching
+    pad_node >= 0) get zero dy and dw rows."""
     import torch
     cp, ce, cr = csc
     _contig(x, y, w, dm)
@@ -309,7 +312,8 @@ def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=Non
     _f32_out(dx, dy, dw)
     _check(load().e3gb_conv_backward(t.handle, N, E, _ptr(cp), _ptr(ce) if E else None, _ptr(cr) if E else None,
                                      _ptr(x), _ptr(y) if E else None, _ptr(w) if E else None, _ptr(dm),
-                                     float(scale), _ptr(dx), _ptr(dy) if E else None, _ptr(dw) if E else None,
+                                     float(scale), int(pad_node), _ptr(dx), _ptr(dy) if E else None,
+                                     _ptr(dw) if E else None,
                                      _dtype(x, dm, *((y, w) if E else ())), _stream(stream)))
     return dx, dy, dw
 

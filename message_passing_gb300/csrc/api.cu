@@ -31,6 +31,9 @@ cudaError_t sh_backward(int lmax, int64_t n, const float* vec, const void* dy, f
 size_t graph_workspace_bytes(int64_t N);
 cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
                           int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s);
+cudaError_t zero_padding_edges(int64_t N, int64_t E, const int32_t* csc_ptr, const int32_t* csc_edge,
+                               const int32_t* csc_recv, int64_t pad, float* dw, int64_t dw_row, float* dy,
+                               int64_t dy_row, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------
 // launch sizing: grid = min(blocks needed, resident blocks per SM x SMs), cached per kernel
@@ -381,10 +384,12 @@ e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const in
 
 e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
                               const int32_t* sender, const void* x, const void* y, const void* w, float scale,
-                              void* m, e3gb_dtype dtype, void* stream) {
+                              int64_t pad_node, void* m, e3gb_dtype dtype, void* stream) {
     E3GB_TRY(check_table(t, dtype));
     if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
     if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (pad_node < -1 || pad_node >= n_nodes)
+        return fail(E3GB_ERR_INVALID_ARG, "pad_node %lld outside [-1, n_nodes)", (long long)pad_node);
     if (n_nodes == 0) {
         if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
         return ok();
@@ -400,18 +405,20 @@ e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_ed
     e3gb_status st = E3GB_OK;
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;
-    return cuda_status(t->ops->conv_fwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m, err,
-                                               (cudaStream_t)stream),
+    return cuda_status(t->ops->conv_fwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m, pad_node,
+                                               err, (cudaStream_t)stream),
                        "conv_forward launch");
 }
 
 e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* csc_ptr,
                                const int32_t* csc_edge, const int32_t* csc_recv, const void* x, const void* y,
-                               const void* w, const void* dm, float scale, void* dx, void* dy, void* dw,
-                               e3gb_dtype dtype, void* stream) {
+                               const void* w, const void* dm, float scale, int64_t pad_node, void* dx, void* dy,
+                               void* dw, e3gb_dtype dtype, void* stream) {
     E3GB_TRY(check_table(t, dtype));
     if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
     if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (pad_node < -1 || pad_node >= n_nodes)
+        return fail(E3GB_ERR_INVALID_ARG, "pad_node %lld outside [-1, n_nodes)", (long long)pad_node);
     if (n_nodes == 0) {
         if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
         return ok();
@@ -431,9 +438,12 @@ e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_e
     e3gb_status st = E3GB_OK;
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;
-    return cuda_status(t->ops->conv_bwd[dtype](n_nodes, n_edges, t->mul, csc_ptr, csc_edge, csc_recv, x, y, w, dm,
-                                               scale, dx, dy, dw, err, (cudaStream_t)stream),
-                       "conv_backward launch");
+    E3GB_TRY(cuda_status(t->ops->conv_bwd[dtype](n_nodes, n_edges, t->mul, csc_ptr, csc_edge, csc_recv, x, y, w,
+                                                 dm, scale, dx, dy, dw, pad_node, err, (cudaStream_t)stream),
+                         "conv_backward launch"));
+    return cuda_status(zero_padding_edges(n_nodes, n_edges, csc_ptr, csc_edge, csc_recv, pad_node, (float*)dw,
+                                          int64_t(t->ops->NP) * t->mul, (float*)dy, t->ops->D2, (cudaStream_t)stream),
+                       "zero_padding_edges launch");
 }
 
 e3gb_status e3gb_check_device_status(void* stream, int32_t* flags) {

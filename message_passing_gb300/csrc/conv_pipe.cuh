@@ -284,7 +284,7 @@ template <class Cfg, class T, int NSLOT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ sender,
                          const T* __restrict__ x, const T* __restrict__ y, const T* __restrict__ w, float scale,
-                         float* __restrict__ m, unsigned* __restrict__ err) {
+                         float* __restrict__ m, int64_t pad, unsigned* __restrict__ err) {
     using F = FwdPipe<Cfg, T, NSLOT>;
     using PP = PipePlan<Cfg>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -300,12 +300,18 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
     int64_t pn = gw, pe = 0, pend = 0;
     int pc = 0;
     bool pdone = false;
-    auto p_seek = [&]() {   // make pe < pend or set pdone
-        while (pe >= pend) {
+    // padding edges (receiver or sender == pad, pad >= 0) are never issued: the padding
+    // receiver's segment is passed over whole, edges from the padding sender one by one
+    auto p_seek = [&]() {   // make pe < pend (pe not a padding edge) or set pdone
+        for (;;) {
+            if (pad >= 0)
+                while (pe < pend && __ldg(sender + pe) == pad) ++pe;
+            if (pe < pend) return;
             if (pn >= N) { pdone = true; return; }
             const int64_t k0 = __ldg(rowptr + pn), k1 = __ldg(rowptr + pn + 1);
+            const bool skip = pn == pad;
             pn += nw;
-            if (seg_ok(k0, k1, E)) { pe = k0; pend = k1; }
+            if (!skip && seg_ok(k0, k1, E)) { pe = k0; pend = k1; }
         }
     };
     auto issue = [&](int64_t i) {   // issue the producer's current item into slot i % NSLOT
@@ -347,11 +353,13 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
             if (lane == 0) atomicOr(err, kErrRowptr);
             e0 = e1 = 0;
         }
+        if (b == pad) e0 = e1 = 0;
         Q2 acc[Cfg::D];
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i) acc[i] = q2_zero();
         for (int64_t e = e0; e < e1; ++e) {
             const int64_t a = __ldg(sender + e);
+            if (pad >= 0 && a == pad) continue;   // not issued by the producer either
             const bool ok = a >= 0 && a < N;
             if (!ok && lane == 0) atomicOr(err, kErrSender);
             Q2 xv[Cfg::D1];
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr, const int32_t* __restrict__ cedge,
                           const int32_t* __restrict__ crecv, const T* __restrict__ x, const T* __restrict__ y,
                           const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
-                          float* __restrict__ dy, float* __restrict__ dw, unsigned* __restrict__ err) {
+                          float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err) {
     using B = BwdPipe<Cfg, T, NSLOT>;
     using PP = PipePlan<Cfg>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -490,13 +498,21 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
     int64_t pa = gw - nw, pk = 0, pkend = 0;
     int pc = 0;
     bool pdone = false;
+    // padding edges (sender or receiver == pad, pad >= 0) are never issued: the padding
+    // sender's segment is passed over whole (only its x item is issued), edges into the
+    // padding receiver one by one
+    auto p_skip_pad = [&]() {
+        if (pad >= 0)
+            while (pk < pkend && __ldg(crecv + pk) == pad) ++pk;
+    };
     auto p_next_sender = [&]() {
         pa += nw;
         if (pa >= N) { pdone = true; return; }
         int64_t k0 = __ldg(cptr + pa), k1 = __ldg(cptr + pa + 1);
-        if (!seg_ok(k0, k1, E)) k0 = k1 = 0;
+        if (!seg_ok(k0, k1, E) || pa == pad) k0 = k1 = 0;
         pk = k0;
         pkend = k1;
+        p_skip_pad();
         pc = -1;
     };
     auto issue = [&](int64_t i) {
@@ -535,7 +551,9 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                 }
                 if (++pc == B::NCH) {
                     pc = 0;
-                    if (++pk >= pkend) p_next_sender();
+                    ++pk;
+                    p_skip_pad();
+                    if (pk >= pkend) p_next_sender();
                 }
             }
         }
@@ -552,6 +570,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             if (lane == 0) atomicOr(err, kErrRowptr);
             k0 = k1 = 0;
         }
+        if (a == pad) k0 = k1 = 0;
         Q2 dxa[Cfg::D1];
         {   // item: x rows of the sender -> the warp's x buffer (each lane its own channels)
             issue(issued++);
@@ -567,6 +586,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
         }
         for (int64_t k = k0; k < k1; ++k) {
             const int64_t e = __ldg(cedge + k), bb = __ldg(crecv + k);
+            if (pad >= 0 && bb == pad) continue;   // not issued by the producer either
             const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
             if (!ok && lane == 0) atomicOr(err, kErrRecv);
             float dyp[Cfg::D2];

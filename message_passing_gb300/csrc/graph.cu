@@ -122,11 +122,57 @@ __global__ void recv_kernel(int64_t N, int64_t K, const int32_t* __restrict__ ro
     }
 }
 
+// Zero the dw and dy rows of every padding edge: the edges into the padding receiver (found
+// by a warp-wide ballot over csc_recv) and the padding sender's edges (its sender-major
+// segment). Each padding edge appears once in the sender-major index, so each row has one
+// writer. Edge ids out of range are left alone (the conv kernel flags them).
+__global__ void zero_padding_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr,
+                                    const int32_t* __restrict__ cedge, const int32_t* __restrict__ crecv,
+                                    int64_t pad, float* __restrict__ dw, int64_t dw_row, float* __restrict__ dy,
+                                    int64_t dy_row) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    int64_t s0 = cptr[pad], s1 = cptr[pad + 1];
+    if (s0 < 0 || s1 < s0 || s1 > E) s0 = s1 = 0;
+    for (int64_t base = gw * 32; base < E; base += nw * 32) {   // warp-uniform trip count
+        const int64_t k = base + lane;
+        int64_t e = -1;
+        if (k < E && (crecv[k] == pad || (k >= s0 && k < s1))) {
+            e = cedge[k];
+            if (e >= E) e = -1;
+        }
+        unsigned todo = __ballot_sync(0xffffffffu, e >= 0);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int64_t ee = __shfl_sync(0xffffffffu, e, src);
+            float* r = dw + ee * dw_row;
+            for (int64_t i = lane; i < dw_row; i += 32) __stcs(r + i, 0.f);
+            for (int64_t i = lane; i < dy_row; i += 32) dy[ee * dy_row + i] = 0.f;
+        }
+    }
+}
+
 inline int grid1d(int64_t n, int block, int cap) {
     const int64_t g = (n + block - 1) / block;
     return int(g < cap ? (g > 0 ? g : 1) : cap);
 }
 }  // namespace
+
+cudaError_t zero_padding_edges(int64_t N, int64_t E, const int32_t* csc_ptr, const int32_t* csc_edge,
+                               const int32_t* csc_recv, int64_t pad, float* dw, int64_t dw_row, float* dy,
+                               int64_t dy_row, cudaStream_t s) {
+    if (E <= 0 || pad < 0 || pad >= N) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t st = cudaGetDevice(&dev);
+    if (st == cudaSuccess) st = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (st != cudaSuccess) return st;
+    const int block = 256;
+    zero_padding_kernel<<<grid1d((E + 7) / 8, block, sms * 8), block, 0, s>>>(N, E, csc_ptr, csc_edge, csc_recv, pad,
+                                                                              dw, dw_row, dy, dy_row);
+    return cudaGetLastError();
+}
 
 size_t graph_workspace_bytes(int64_t N) { return size_t((N + 1) * 4 + 255) / 256 * 256; }
 

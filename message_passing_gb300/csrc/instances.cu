@@ -48,11 +48,12 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
                    void* dy, void* dw, cudaStream_t s);
 template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                     const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s);
+                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                     cudaStream_t s);
 template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
-                     void* dw, unsigned* err, cudaStream_t s);
+                     void* dw, int64_t pad, unsigned* err, cudaStream_t s);
 
 #if E3GB_PART == 0
 template <class T>
@@ -83,7 +84,8 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
 #if E3GB_PART == 0
 template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                     const void* y, const void* w, float scale, void* m, unsigned* err, cudaStream_t s) {
+                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                     cudaStream_t s) {
     using S = PipeShape<Cfg, T, false>;
     if constexpr (S::usable) {
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w)) {
@@ -94,7 +96,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale,
-                                                   (float*)m, err);
+                                                   (float*)m, pad, err);
             return cudaGetLastError();
         }
     }
@@ -102,7 +104,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
-                              err);
+                              pad, err);
     return cudaGetLastError();
 }
 
@@ -112,7 +114,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
 template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
-                     void* dw, unsigned* err, cudaStream_t s) {
+                     void* dw, int64_t pad, unsigned* err, cudaStream_t s) {
     using S = PipeShape<Cfg, T, true>;
     if constexpr (S::usable) {
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm)) {
@@ -123,7 +125,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                                                   (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, err);
+                                                   (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err);
             return cudaGetLastError();
         }
     }
@@ -131,7 +133,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                              (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, err);
+                              (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err);
     return cudaGetLastError();
 }
 
@@ -141,10 +143,10 @@ template cudaError_t tp_bwd<__nv_bfloat16>(int64_t, int, const void*, const void
                                             void*, void*, cudaStream_t);
 template cudaError_t conv_bwd<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
                                       const void*, const void*, const void*, const void*, float, void*, void*, void*,
-                                      unsigned*, cudaStream_t);
+                                      int64_t, unsigned*, cudaStream_t);
 template cudaError_t conv_bwd<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
                                               const void*, const void*, const void*, const void*, float, void*, void*,
-                                              void*, unsigned*, cudaStream_t);
+                                              void*, int64_t, unsigned*, cudaStream_t);
 #endif  // part 1
 }  // namespace cfg<id>
 

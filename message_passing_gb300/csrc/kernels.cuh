@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
                                                            const int32_t* __restrict__ sender,
                                                            const T* __restrict__ x, const T* __restrict__ y,
                                                            const T* __restrict__ w, float scale,
-                                                           float* __restrict__ m, unsigned* __restrict__ err) {
+                                                           float* __restrict__ m, int64_t pad,
+                                                           unsigned* __restrict__ err) {
     const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -399,8 +400,10 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
             if (L.gl == 0) atomicOr(err, kErrRowptr);
             e1 = e0 = 0;
         }
+        if (b == pad) e0 = e1 = 0;   // padding receiver: no messages
         for (int64_t e = e0; e < e1; ++e) {
             const int64_t a = __ldg(sender + e);
+            if (pad >= 0 && a == pad) continue;   // padding edge
             if (a < 0 || a >= N) {
                 if (L.gl == 0) atomicOr(err, kErrSender);
                 continue;
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
     int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
     const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y,
     const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
-    float* __restrict__ dy, float* __restrict__ dw, unsigned* __restrict__ err) {
+    float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err) {
     const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -468,6 +471,7 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
                 if (L.gl == 0) atomicOr(err, kErrRowptr);
                 k0 = k1 = 0;
             }
+            if (aa == pad) k0 = k1 = 0;   // padding sender: no messages
         }
         // the row groups of a warp may own different edge counts; loop to the warp maximum
         int64_t cnt = k1 - k0, wmax = cnt;
@@ -481,7 +485,9 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
             if (ok) {
                 e = __ldg(csc_edge + k0 + i);
                 b = __ldg(csc_recv + k0 + i);
-                if (e < 0 || e >= E || b < 0 || b >= N) {
+                if (pad >= 0 && b == pad) {
+                    ok = false;   // padding edge: its dw, dy rows are zeroed separately
+                } else if (e < 0 || e >= E || b < 0 || b >= N) {
                     if (L.gl == 0) atomicOr(err, kErrRecv);
                     ok = false;
                 }
@@ -526,10 +532,10 @@ struct ConfigOps {
     cudaError_t (*tp_bwd[2])(int64_t, int, const void*, const void*, const void*, const void*, void*, void*,
                              void*, cudaStream_t);
     cudaError_t (*conv_fwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
-                               const void*, const void*, float, void*, unsigned*, cudaStream_t);
+                               const void*, const void*, float, void*, int64_t, unsigned*, cudaStream_t);
     cudaError_t (*conv_bwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
                                const void*, const void*, const void*, const void*, float, void*, void*,
-                               void*, unsigned*, cudaStream_t);
+                               void*, int64_t, unsigned*, cudaStream_t);
 };
 
 int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units);

@@ -138,13 +138,29 @@ def _segments(ptr, ids):
     return sub, edges
 
 
-def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, receivers=None):
+def _drop_padding(sub, edges, owner, other, pad):
+    """Remove the padding edges from per-node edge lists (sub offsets, edges ids): an edge is
+    padding when its owning node (owner[i] for list position i) or its other end (other[i])
+    is the padding node. e3j, Sec. 4 "Message passing convolution" and App. E: static-shape
+    graphs send their unused edge slots to one padding node, and the kernels skip them."""
+    if pad is None or pad < 0:
+        return sub, edges
+    keep = (owner != pad) & (other != pad)
+    seg = np.repeat(np.arange(len(sub) - 1), np.diff(sub))      # list position -> node slot
+    kept = np.zeros(len(sub), dtype=np.int64)
+    np.cumsum(np.bincount(seg[keep], minlength=len(sub) - 1), out=kept[1:])
+    return kept, edges[keep]
+
+
+def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, receivers=None, pad_node=None):
     """m[len(receivers), D, Nq] = scale * sum over each receiver's CSR edges (Eq. 12-13).
-    y and w are per-edge arrays over all edges (or callables edge_ids -> rows)."""
+    y and w are per-edge arrays over all edges (or callables edge_ids -> rows). With pad_node,
+    the edges whose receiver or sender is pad_node contribute nothing."""
     rowptr = np.asarray(rowptr, dtype=np.int64)
     n = rowptr.shape[0] - 1
     recv = np.arange(n) if receivers is None else np.asarray(receivers, dtype=np.int64)
     sub, edges = _segments(rowptr, recv)
+    sub, edges = _drop_padding(sub, edges, np.repeat(recv, np.diff(sub)), np.asarray(sender)[edges], pad_node)
     snd = np.ascontiguousarray(np.asarray(sender)[edges], dtype=np.int32)
     ye = _f64(y(edges) if callable(y) else np.asarray(y)[edges])
     we = _f64(w(edges) if callable(w) else np.asarray(w)[edges])
@@ -162,11 +178,21 @@ def receivers_of(rowptr) -> np.ndarray:
     return np.repeat(np.arange(rowptr.shape[0] - 1, dtype=np.int32), np.diff(rowptr))
 
 
-def conv_backward_edges(t: Table, rowptr, sender, x, y, w, dm, scale: float, edges=None):
-    """(dy[len(edges), d2], dw[len(edges), P, Nq]) for the given edge ids (Eq. 16)."""
+def conv_backward_edges(t: Table, rowptr, sender, x, y, w, dm, scale: float, edges=None, pad_node=None):
+    """(dy[len(edges), d2], dw[len(edges), P, Nq]) for the given edge ids (Eq. 16). A padding
+    edge (receiver or sender == pad_node) takes no part in the forward, so both are zero."""
     sender = np.asarray(sender)
     E = sender.shape[0]
     edges = np.arange(E) if edges is None else np.asarray(edges, dtype=np.int64)
+    if pad_node is not None and pad_node >= 0:
+        rcv = receivers_of(rowptr)[edges]
+        real = (rcv != pad_node) & (sender[edges] != pad_node)
+        Nq = np.asarray(x).shape[2]
+        dy = np.zeros((len(edges), t.d2))
+        dw = np.zeros((len(edges), t.n_paths, Nq))
+        if real.any():
+            dy[real], dw[real] = conv_backward_edges(t, rowptr, sender, x, y, w, dm, scale, edges[real])
+        return dy, dw
     recv = receivers_of(rowptr)[edges]
     snd = np.ascontiguousarray(sender[edges], dtype=np.int32)
     ye = _f64(y(edges) if callable(y) else np.asarray(y)[edges])
@@ -182,8 +208,9 @@ def conv_backward_edges(t: Table, rowptr, sender, x, y, w, dm, scale: float, edg
     return dy, dw
 
 
-def conv_backward_dx(t: Table, rowptr, sender, y, w, dm, scale: float, senders=None, Nq=None):
-    """dx[len(senders), d1, Nq]: sum over the edges whose sender is each node (Eq. 16)."""
+def conv_backward_dx(t: Table, rowptr, sender, y, w, dm, scale: float, senders=None, Nq=None, pad_node=None):
+    """dx[len(senders), d1, Nq]: sum over the edges whose sender is each node (Eq. 16); with
+    pad_node, over the edges that are not padding (receiver and sender != pad_node)."""
     sender = np.asarray(sender, dtype=np.int64)
     n = np.asarray(rowptr).shape[0] - 1
     dm = _f64(dm)
@@ -196,6 +223,7 @@ def conv_backward_dx(t: Table, rowptr, sender, y, w, dm, scale: float, senders=N
     np.cumsum(np.bincount(sender, minlength=n), out=cptr[1:])
     sub, pos = _segments(cptr, nodes)
     edges = order[pos]
+    sub, edges = _drop_padding(sub, edges, np.repeat(nodes, np.diff(sub)), recv_all[edges], pad_node)
     ye = _f64(y(edges) if callable(y) else np.asarray(y)[edges])
     we = _f64(w(edges) if callable(w) else np.asarray(w)[edges])
     pinfo, cg = _pack(t)

@@ -231,6 +231,37 @@ def random_graph(n_nodes: int, n_edges: int, key: tuple[int, ...], empty_nodes: 
     return Graph(n_nodes, rowptr.astype(np.int32), send.astype(np.int32), vec, 0.0, 0.0, "random")
 
 
+def padded_graph(g: Graph, n_self: int, n_out: int, n_in: int, key: tuple[int, ...]):
+    """g plus one padding node (index g.n_nodes) and padding edges, the static-shape layout of
+    JAX graph codes (e3j, Sec. 4 "Message passing convolution": unused edge slots all point at
+    one padding node). n_self edges pad -> pad, n_out edges pad -> a random real receiver,
+    n_in edges a random real sender -> pad. Padding edges are placed at random positions
+    inside their receiver's segment; real edges keep their relative order. Returns
+    (graph, pad, orig): orig[e] is the index in g of new edge e, or -1 for padding edges.
+    Padding edge vectors are NaN."""
+    r = rng(*key)
+    N, pad = g.n_nodes, g.n_nodes
+    recv0 = g.receiver().astype(np.int64)
+    deg = np.diff(g.rowptr.astype(np.int64))
+    rank = np.arange(g.n_edges) - np.repeat(g.rowptr[:-1].astype(np.int64), deg)
+    p_recv = np.concatenate([np.full(n_self, pad), r.integers(0, N, n_out), np.full(n_in, pad)]).astype(np.int64)
+    p_send = np.concatenate([np.full(n_self, pad), np.full(n_out, pad), r.integers(0, N, n_in)]).astype(np.int64)
+    degp = np.concatenate([deg, [0]])
+    p_posn = r.uniform(-0.5, degp[p_recv] + 0.5)
+    recv = np.concatenate([recv0, p_recv])
+    send = np.concatenate([g.sender.astype(np.int64), p_send])
+    posn = np.concatenate([rank.astype(np.float64), p_posn])
+    orig = np.concatenate([np.arange(g.n_edges), np.full(len(p_recv), -1)])
+    srt = np.lexsort((posn, recv))
+    recv, send, orig = recv[srt], send[srt], orig[srt]
+    rowptr = np.zeros(N + 2, dtype=np.int64)
+    np.cumsum(np.bincount(recv, minlength=N + 1), out=rowptr[1:])
+    vec = np.full((len(orig), 3), np.nan)
+    vec[orig >= 0] = g.vec[orig[orig >= 0]]
+    out = Graph(N + 1, rowptr.astype(np.int32), send.astype(np.int32), vec, g.box, g.cutoff, g.order + "+pad")
+    return out, pad, orig
+
+
 def device_normal(shape: tuple[int, ...], key: tuple[int, ...], scale: float = 1.0, device="cuda",
                   dtype=None):
     """Seeded N(0, scale^2) float32 tensor drawn on the GPU with torch's generator (for inputs

@@ -88,8 +88,15 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert b"NULL" in lib.e3gb_last_error()
     assert lib.e3gb_tp_forward(t.handle.value, -1, None, None, None, None, 0, None) == e3.ERR_INVALID_ARG
     assert lib.e3gb_tp_forward(t.handle.value, 4, None, None, None, None, 7, None) == e3.ERR_INVALID_ARG
-    assert lib.e3gb_conv_forward(t.handle.value, 0, 5, None, None, None, None, None, ctypes.c_float(1.0), None,
-                                 0, None) == e3.ERR_BAD_GRAPH
+    assert lib.e3gb_conv_forward(t.handle.value, 0, 5, None, None, None, None, None, ctypes.c_float(1.0), -1,
+                                 None, 0, None) == e3.ERR_BAD_GRAPH
+    # the padding node must be a node (or -1 for none)
+    for pad in (-2, 4, 100):
+        assert lib.e3gb_conv_forward(t.handle.value, 4, 5, None, None, None, None, None, ctypes.c_float(1.0), pad,
+                                     None, 0, None) == e3.ERR_INVALID_ARG
+        assert b"pad_node" in lib.e3gb_last_error()
+        assert lib.e3gb_conv_backward(t.handle.value, 4, 5, None, None, None, None, None, None, None,
+                                      ctypes.c_float(1.0), pad, None, None, None, 0, None) == e3.ERR_INVALID_ARG
     assert lib.e3gb_sh_forward(4, 3, None, None, 0, None) == e3.ERR_UNSUPPORTED
     assert lib.e3gb_graph_prepare(10, 20, None, None, None, None, None, None, 0, None) == e3.ERR_INVALID_ARG
     assert lib.e3gb_graph_prepare_workspace_bytes(1000) >= 1001 * 4
