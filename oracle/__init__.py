@@ -235,5 +235,37 @@ def conv_backward_dx(t: Table, rowptr, sender, y, w, dm, scale: float, senders=N
     return dx
 
 
+def conv_double_backward(t: Table, rowptr, sender, x, y, w, dm, ddx, ddy, ddw, scale: float,
+                         receivers=None, senders=None, edges=None, pad_node=None):
+    """Second-order rule of the convolution, e3j App. E.1 Eq. (17)-(18): with (ddx, ddy, ddw)
+    the variations of the cotangents (dx, dy, dw) returned by the backward pass,
+
+      delta dm = conv(ddx, y, w) + conv(x, ddy, w) + conv(x, y, ddw)                     (17)
+      (-, dx_y, dx_w) = conv_bwd(ddx, y, w, dm)                                          (18)
+      (dy_x, -, dy_w) = conv_bwd(x, ddy, w, dm)
+      (dw_x, dw_y, -) = conv_bwd(x, y, ddw, dm)
+      delta x = dy_x + dw_x,  delta y = dx_y + dw_y,  delta w = dx_w + dy_w
+
+    (the table's labels: each conv_bwd call returns (dx, dy, dw) of its own arguments).
+    Returns (delta_x[senders], delta_y[edges], delta_w[edges], delta_dm[receivers]).
+    y, w, ddy, ddw may be callables edge_ids -> rows."""
+    sender = np.asarray(sender)
+    n = np.asarray(rowptr).shape[0] - 1
+    Nq = np.asarray(x).shape[2]
+    kw = dict(pad_node=pad_node)
+    # (17)
+    ddm = (conv_forward(t, rowptr, sender, ddx, y, w, scale, receivers, **kw)
+           + conv_forward(t, rowptr, sender, x, ddy, w, scale, receivers, **kw)
+           + conv_forward(t, rowptr, sender, x, y, ddw, scale, receivers, **kw))
+    # (18): the three conv_bwd calls, each with one primal replaced by its variation
+    dy1, dw1 = conv_backward_edges(t, rowptr, sender, ddx, y, w, dm, scale, edges, **kw)
+    dx2 = conv_backward_dx(t, rowptr, sender, ddy, w, dm, scale, senders, Nq, **kw)
+    _, dw2 = conv_backward_edges(t, rowptr, sender, x, ddy, w, dm, scale, edges, **kw)
+    dx3 = conv_backward_dx(t, rowptr, sender, y, ddw, dm, scale, senders, Nq, **kw)
+    dy3, _ = conv_backward_edges(t, rowptr, sender, x, y, ddw, dm, scale, edges, **kw)
+    return dx2 + dx3, dy1 + dy3, dw1 + dw2, ddm
+
+
 __all__ = ["sh", "sh_grad", "cg_block", "table", "tp_forward", "tp_backward", "conv_forward",
-           "conv_backward_edges", "conv_backward_dx", "build", "num_threads", "receivers_of"]
+           "conv_backward_edges", "conv_backward_dx", "conv_double_backward", "build", "num_threads",
+           "receivers_of"]
