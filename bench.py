@@ -304,6 +304,66 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
     return out
 
 
+def dbwd_bytes(N, E, d1, d2, P, D, Nq, s):
+    """Algorithmic bytes of the double backward (Eq. 9 accounting): primals x, y, w, dm and
+    the variations ddx, ddy, ddw in; delta_x, delta_y, delta_w, delta_dm out (fp32); both
+    graph indices."""
+    return (2 * (N * d1 * Nq + E * d2 + E * P * Nq) * s + N * D * Nq * s
+            + 2 * (N + 1) * 4 + 3 * E * 4
+            + (N * d1 * Nq + E * d2 + E * P * Nq + N * D * Nq) * 4)
+
+
+def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float):
+    """Device time of the fused double backward (Eq. 17-18) on a conv workload, and of the
+    pages' formulation beside it: three conv and three conv_bwd calls (their three output
+    additions not counted)."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import STREAM_GRAD, STREAM_W, device_normal
+    from synth import workloads as W
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    g = W.make_graph(wl)
+    N, E, Nq, P, D = g.n_nodes, g.n_edges, wl.mul, t.n_paths, t.D
+    scale = N / E
+    x_np, _ = W.make_conv(wl, g, P, edge_ids=np.zeros(0, np.int64))
+    xd = torch.from_numpy(x_np).to(dev)
+    ddx = torch.from_numpy(np.ascontiguousarray(x_np[::-1])).to(dev)
+    rp = torch.from_numpy(g.rowptr).to(dev)
+    sd = torch.from_numpy(g.sender).to(dev)
+    y = e3.sh_forward(torch.from_numpy(g.vec.astype(np.float32)).to(dev), wl.sh_lmax)
+    ddy = torch.flip(y, dims=(0,)).contiguous()
+    wd = device_normal((E, P, Nq), (wl.wid, STREAM_W), W.weight_scale(wl, P), device=dev)
+    ddw = device_normal((E, P, Nq), (wl.wid, STREAM_W, 1), W.weight_scale(wl, P), device=dev)
+    dmd = device_normal((N, D, Nq), (wl.wid, STREAM_GRAD), device=dev)
+    csc = e3.graph_prepare(rp, sd, N)
+    f32 = dict(dtype=torch.float32)
+    out = (torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd), torch.empty_like(dmd))
+    tmp_m = torch.empty((N, D, Nq), device=dev, **f32)
+    tmp_b = (torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        ev[k][0].record(stream)
+        e3.conv_double_backward(t, rp, sd, csc, xd, y, wd, dmd, ddx, ddy, ddw, scale, out=out, stream=stream)
+        ev[k][1].record(stream)
+        for a_, b_, c_ in ((ddx, y, wd), (xd, ddy, wd), (xd, y, ddw)):
+            e3.conv_forward(t, rp, sd, a_, b_, c_, scale, out=tmp_m, stream=stream)
+            e3.conv_backward(t, csc, a_, b_, c_, dmd, scale, out=tmp_b, stream=stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    e3.check_device_status()
+    tf = _median([e[0].elapsed_time(e[1]) for e in ev[2:]]) / 1e3
+    tc = _median([e[1].elapsed_time(e[2]) for e in ev[2:]]) / 1e3
+    bb = dbwd_bytes(N, E, t.d1, t.d2, P, D, Nq, 4)
+    res = {"workload": wl.name, "dtype": "f32", "atoms": N, "edges": E,
+           "fused": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bb / tf / 1e9, "frac": bb / tf / 1e9 / hbm_peak},
+           "composition_six_calls": {"ms": tc * 1e3, "edges_per_s": E / tc},
+           "speedup_vs_composition": tc / tf}
+    del xd, ddx, y, ddy, wd, ddw, dmd, out, tmp_m, tmp_b
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_tp_workload(wl, dev, stream, reps: int, hbm_peak: float):
     """Per-kernel device times of TP forward and backward on a row workload (fp32)."""
     import torch
@@ -524,7 +584,7 @@ def run_ours(args):
                "includes": "pinned H2D of vec, rowptr, sender, x, w, dm; SH; graph_prepare; conv fwd; conv bwd; D2H of m, dx, dy, dw"}
         del h_w, o_dw
     # ---- the other workloads (kernel times only; rank 0)
-    others = None
+    others = double_bwd = None
     if rank == 0 and not args.no_workloads:
         del wd, dmd, dx, dy, dw, xd, y, m
         torch.cuda.empty_cache()
@@ -534,6 +594,7 @@ def run_ours(args):
                   time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak, pad_frac=0.25)]
+        double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -560,7 +621,8 @@ def run_ours(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if bf16 else "f32", "data": "synthetic", "config": workload_config(w, g, args),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps,
-                "clocks": clk, "rows": rows, "tp": tp, "workloads": others}
+                "clocks": clk, "rows": rows, "tp": tp, "workloads": others,
+                "double_backward": double_bwd}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

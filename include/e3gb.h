@@ -202,6 +202,30 @@ e3gb_status e3gb_conv_backward(const e3gb_table *t, int64_t n_nodes, int64_t n_e
                                const void *w, const void *dm, float scale, int64_t pad_node,
                                void *dx, void *dy, void *dw, e3gb_dtype dtype, void *stream);
 
+/* Double backward of the convolution (e3j App. E.1 Eq. (17)-(18)). Given the primals x, y,
+ * w, dm of e3gb_conv_backward and variations delta_dx [n_nodes,d1,Nq], delta_dy
+ * [n_edges,d2], delta_dw [n_edges,P,Nq] of the cotangents it returned, computes the
+ * gradient of <dx, delta_dx> + <dy, delta_dy> + <dw, delta_dw> with respect to the primals:
+ *   delta_dm = conv(delta_dx, y, w) + conv(x, delta_dy, w) + conv(x, y, delta_dw)   (17)
+ *   delta_x  = dx of conv_bwd(x, delta_dy, w, dm) + dx of conv_bwd(x, y, delta_dw, dm)
+ *   delta_y  = dy of conv_bwd(delta_dx, y, w, dm) + dy of conv_bwd(x, y, delta_dw, dm)
+ *   delta_w  = dw of conv_bwd(delta_dx, y, w, dm) + dw of conv_bwd(x, delta_dy, w, dm)   (18)
+ * in two fused launches (a receiver-ordered pass for delta_dm over rowptr/sender, a
+ * sender-ordered pass for the rest over csc_* from e3gb_graph_prepare) that compute none of
+ * the cotangents Eq. (18) discards. delta_x [n_nodes,d1,Nq], delta_y [n_edges,d2], delta_w
+ * [n_edges,P,Nq], delta_dm [n_nodes,D,Nq], fp32, fully overwritten; deterministic (fixed
+ * summation order, no atomics). scale and pad_node as in e3gb_conv_forward (padding edges
+ * get zero delta_y, delta_w rows). Inputs share one dtype. */
+e3gb_status e3gb_conv_double_backward(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                                      const int32_t *rowptr, const int32_t *sender,
+                                      const int32_t *csc_ptr, const int32_t *csc_edge,
+                                      const int32_t *csc_recv, const void *x, const void *y,
+                                      const void *w, const void *dm, const void *delta_dx,
+                                      const void *delta_dy, const void *delta_dw, float scale,
+                                      int64_t pad_node, void *delta_x, void *delta_y,
+                                      void *delta_w, void *delta_dm, e3gb_dtype dtype,
+                                      void *stream);
+
 /* Synchronise stream, read and clear the device error word of the current device.
  * E3GB_OK when clean, E3GB_ERR_DEVICE_INDEX when a kernel skipped bad indices (*flags, if
  * not NULL, receives the bits: 1 bad sender, 2 bad CSR pointer, 4 bad receiver / edge id). */

@@ -28,6 +28,7 @@ SYMBOLS = (
     "e3gb_sh_backward",
     "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
     "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
+    "e3gb_conv_double_backward",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
 )
 
@@ -74,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_graph_prepare_static": (i32, [i64, i64, vp, vp, vp, vp, vp, vp]),
         "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, i64, vp, i32, vp]),
         "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, i64, vp, vp, vp, i32, vp]),
+        "e3gb_conv_double_backward": (i32, [vp, i64, i64] + [vp] * 5 + [vp] * 7 + [f32, i64] + [vp] * 4
+                                      + [i32, vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
         "e3gb_last_error": (ctypes.c_char_p, []),
         "e3gb_version": (ctypes.c_char_p, []),
@@ -316,6 +319,28 @@ def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=Non
                                      _ptr(dw) if E else None,
                                      _dtype(x, dm, *((y, w) if E else ())), _stream(stream)))
     return dx, dy, dw
+
+
+def conv_double_backward(t: Table, rowptr, sender, csc, x, y, w, dm, delta_dx, delta_dy, delta_dw, scale: float,
+                         out=None, stream=None, pad_node: int = -1):
+    """Eq. (17)-(18): returns (delta_x, delta_y, delta_w, delta_dm), the gradient of
+    <dx, delta_dx> + <dy, delta_dy> + <dw, delta_dw> over (x, y, w, dm)."""
+    import torch
+    cp, ce, cr = csc
+    _contig(rowptr, sender, x, y, w, dm, delta_dx, delta_dy, delta_dw)
+    N, E = x.shape[0], y.shape[0]
+    if out is None:
+        f = dict(dtype=torch.float32)
+        out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f),
+               torch.empty_like(dm, **f))
+    gx, gy, gw, gdm = out
+    _f32_out(gx, gy, gw, gdm)
+    e = (lambda a: _ptr(a) if E else None)
+    _check(load().e3gb_conv_double_backward(
+        t.handle, N, E, _ptr(rowptr), e(sender), _ptr(cp), e(ce), e(cr), _ptr(x), e(y), e(w), _ptr(dm),
+        _ptr(delta_dx), e(delta_dy), e(delta_dw), float(scale), int(pad_node), _ptr(gx), e(gy), e(gw), _ptr(gdm),
+        _dtype(x, dm, delta_dx, *((y, w, delta_dy, delta_dw) if E else ())), _stream(stream)))
+    return gx, gy, gw, gdm
 
 
 def check_device_status(stream=None) -> int:

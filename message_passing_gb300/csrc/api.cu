@@ -446,6 +446,52 @@ e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_e
                        "zero_padding_edges launch");
 }
 
+e3gb_status e3gb_conv_double_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
+                                      const int32_t* sender, const int32_t* csc_ptr, const int32_t* csc_edge,
+                                      const int32_t* csc_recv, const void* x, const void* y, const void* w,
+                                      const void* dm, const void* delta_dx, const void* delta_dy, const void* delta_dw,
+                                      float scale, int64_t pad_node, void* delta_x, void* delta_y, void* delta_w,
+                                      void* delta_dm, e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (pad_node < -1 || pad_node >= n_nodes)
+        return fail(E3GB_ERR_INVALID_ARG, "pad_node %lld outside [-1, n_nodes)", (long long)pad_node);
+    if (n_nodes == 0) {
+        if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+        return ok();
+    }
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, edges));
+    E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
+    E3GB_TRY(check_ptr(csc_edge, "csc_edge", 4, edges));
+    E3GB_TRY(check_ptr(csc_recv, "csc_recv", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, edges));
+    E3GB_TRY(check_ptr(w, "w", va, edges));
+    E3GB_TRY(check_ptr(dm, "dm", va, true));
+    E3GB_TRY(check_ptr(delta_dx, "delta_dx", va, true));
+    E3GB_TRY(check_ptr(delta_dy, "delta_dy", ea, edges));
+    E3GB_TRY(check_ptr(delta_dw, "delta_dw", va, edges));
+    E3GB_TRY(check_ptr(delta_x, "delta_x", 16, true));
+    E3GB_TRY(check_ptr(delta_y, "delta_y", 4, edges));
+    E3GB_TRY(check_ptr(delta_w, "delta_w", 16, edges));
+    E3GB_TRY(check_ptr(delta_dm, "delta_dm", 16, true));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    E3GB_TRY(cuda_status(t->ops->conv_dbwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, csc_ptr, csc_edge,
+                                                  csc_recv, x, y, w, dm, delta_dx, delta_dy, delta_dw, scale, delta_x,
+                                                  delta_y, delta_w, delta_dm, pad_node, err, (cudaStream_t)stream),
+                         "conv_double_backward launch"));
+    return cuda_status(zero_padding_edges(n_nodes, n_edges, csc_ptr, csc_edge, csc_recv, pad_node, (float*)delta_w,
+                                          int64_t(t->ops->NP) * t->mul, (float*)delta_y, t->ops->D2,
+                                          (cudaStream_t)stream),
+                       "zero_padding_edges launch");
+}
+
 e3gb_status e3gb_check_device_status(void* stream, int32_t* flags) {
     if (flags) *flags = 0;
     e3gb_status st = E3GB_OK;

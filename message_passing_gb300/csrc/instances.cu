@@ -1,11 +1,12 @@
-// One irreps configuration's kernels and launchers; compiled twice per entry of configs.def,
+// One irreps configuration's kernels and launchers; compiled three times per entry of configs.def,
 // with -DE3GB_CFG=<id> -DE3GB_PART=0 (forward kernels and the ops table e3gb::ops_<id>())
-// and -DE3GB_PART=1 (backward kernels), so that the two halves compile in parallel.
+// -DE3GB_PART=1 (backward kernels) and -DE3GB_PART=2 (double backward), so that the three
+// parts compile in parallel.
 #include "conv_pipe.cuh"
 #include "kernels.cuh"
 
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
-#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1>"
+#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2>"
 #endif
 #define E3GB_CAT2(a, b) a##b
 #define E3GB_CAT(a, b) E3GB_CAT2(a, b)
@@ -54,6 +55,11 @@ template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
                      void* dw, int64_t pad, unsigned* err, cudaStream_t s);
+template <class T>
+cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
+                      const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
+                      const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
+                      void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s);
 
 #if E3GB_PART == 0
 template <class T>
@@ -148,6 +154,36 @@ template cudaError_t conv_bwd<__nv_bfloat16>(int64_t, int64_t, int, const int32_
                                               const void*, const void*, const void*, const void*, float, void*, void*,
                                               void*, int64_t, unsigned*, cudaStream_t);
 #endif  // part 1
+#if E3GB_PART == 2
+template <class T>
+cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
+                      const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
+                      const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
+                      void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s) {
+    auto kr = vec_for(Nq) == 4 ? conv_ddm_kernel<Cfg, T, 4> : conv_ddm_kernel<Cfg, T, 1>;
+    const int gr = grid_for((const void*)kr, kBlock, rows_per_block(Nq), N);
+    if (gr == 0) return cudaSuccess;
+    kr<<<gr, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, (const T*)ddx,
+                             (const T*)ddy, (const T*)ddw, scale, (float*)gdm, pad, err);
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+    auto ks = vec_for(Nq) == 4 ? conv_dbwd_kernel<Cfg, T, 4> : conv_dbwd_kernel<Cfg, T, 1>;
+    const int gs = grid_for((const void*)ks, kBlock, rows_per_block(Nq), N);
+    ks<<<gs, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w, (const T*)dm,
+                             (const T*)ddx, (const T*)ddy, (const T*)ddw, scale, (float*)gx, (float*)gy, (float*)gw,
+                             pad, err);
+    return cudaGetLastError();
+}
+
+template cudaError_t conv_dbwd<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                       const int32_t*, const int32_t*, const void*, const void*, const void*,
+                                       const void*, const void*, const void*, const void*, float, void*, void*, void*,
+                                       void*, int64_t, unsigned*, cudaStream_t);
+template cudaError_t conv_dbwd<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                               const int32_t*, const int32_t*, const void*, const void*, const void*,
+                                               const void*, const void*, const void*, const void*, float, void*,
+                                               void*, void*, void*, int64_t, unsigned*, cudaStream_t);
+#endif  // part 2
 }  // namespace cfg<id>
 
 #if E3GB_PART == 0
@@ -161,6 +197,7 @@ const ConfigOps kOps = {
     {tp_bwd<float>, tp_bwd<__nv_bfloat16>},
     {conv_fwd<float>, conv_fwd<__nv_bfloat16>},
     {conv_bwd<float>, conv_bwd<__nv_bfloat16>},
+    {conv_dbwd<float>, conv_dbwd<__nv_bfloat16>},
 };
 }  // namespace
 

@@ -514,6 +514,272 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
+// Convolution double backward ("e3j ...", App. E.1 Eq. (17)-(18)) in two fused passes
+// instead of three conv and three conv_bwd calls: no cotangent that Eq. (18) discards is
+// computed, and each primal is streamed once per pass.
+//
+// Receiver pass (Eq. 17): delta_dm[b] = scale * sum_e [TP(ddx_a, y, w) + TP(x_a, ddy, w)
+//                                                      + TP(x_a, y, ddw)].
+// Sender pass (Eq. 18), with g = scale * dm[b] and, per path, the adjoint couplings
+//   gy[m1] = sum_m3 A_p(y)[m3][m1] g[m3],   gd[m1] = sum_m3 A_p(ddy)[m3][m1] g[m3]:
+//   delta_x[a]       += w_p gd + ddw_p gy
+//   delta_w[e][p]     = sum_m1 ddx[m1] gy[m1] + x[m1] gd[m1]
+//   delta_y[e][m2]   += sum_{records (m1,m2,m3,c)} c * sum_q (ddx[m1] w_p + x[m1] ddw_p) g[m3]
+// The x and ddx rows of a path's l1 block are loaded per path (L1-resident), which keeps
+// the accumulators in registers at four channels per lane.
+// ------------------------------------------------------------------------------------------
+// acc[row0 + m3][c] += w[c] * sum_m1 A[m3][m1] xr[m1][c] (xr: the path's l1 rows only)
+template <class Cfg, int P, int NROWS, int V>
+__device__ __forceinline__ void tp_rows_acc(const float (&A)[Off<Cfg>::a[P + 1] - Off<Cfg>::a[P]],
+                                            const float (&xr)[2 * Cfg::table.paths[P].l1 + 1][V],
+                                            const float (&wv)[V], float (&acc)[NROWS][V], int row0) {
+    constexpr int a0 = Off<Cfg>::a[P];
+    constexpr int na = Off<Cfg>::a[P + 1] - a0;
+    constexpr int n3 = 2 * Cfg::table.paths[P].l3 + 1;
+    float t[n3][V];
+#pragma unroll
+    for (int m = 0; m < n3; ++m)
+#pragma unroll
+        for (int c = 0; c < V; ++c) t[m][c] = 0.f;
+    sfor<na>([&](auto k) {
+        constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+#pragma unroll
+        for (int c = 0; c < V; ++c) t[e.m3][c] = fmaf(A[decltype(k)::value], xr[e.m1][c], t[e.m3][c]);
+    });
+#pragma unroll
+    for (int m = 0; m < n3; ++m)
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[row0 + m][c] = fmaf(wv[c], t[m][c], acc[row0 + m][c]);
+}
+
+// One output block at a time (the receiver's edge list is walked once per block, the edge
+// rows of a block's paths read once), so only that block's rows are accumulated.
+template <class Cfg, class T, int V>
+__global__ void __launch_bounds__(256) conv_ddm_kernel(int64_t N, int64_t E, int Nq, const int32_t* __restrict__ rowptr,
+                                                       const int32_t* __restrict__ sender, const T* __restrict__ x,
+                                                       const T* __restrict__ y, const T* __restrict__ w,
+                                                       const T* __restrict__ ddx, const T* __restrict__ ddy,
+                                                       const T* __restrict__ ddw, float scale,
+                                                       float* __restrict__ ddm, int64_t pad,
+                                                       unsigned* __restrict__ err) {
+    const Lanes L = lanes_for<V>(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * V;
+    for (int64_t b = warp * L.per_warp + L.grp; b < N; b += nwarp * L.per_warp) {
+        int64_t e0 = __ldg(rowptr + b), e1 = __ldg(rowptr + b + 1);
+        if (e0 < 0 || e1 < e0 || e1 > E) {
+            if (L.gl == 0) atomicOr(err, kErrRowptr);
+            e1 = e0 = 0;
+        }
+        if (b == pad) e0 = e1 = 0;
+        sfor<Cfg::NOUT>([&](auto jj) {
+            constexpr int j = decltype(jj)::value;
+            constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
+            float acc[nrow][V];
+#pragma unroll
+            for (int i = 0; i < nrow; ++i)
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[i][c] = 0.f;
+            for (int64_t e = e0; e < e1; ++e) {
+                const int64_t a = __ldg(sender + e);
+                if (pad >= 0 && a == pad) continue;
+                if (a < 0 || a >= N) {
+                    if (j == 0 && L.gl == 0) atomicOr(err, kErrSender);
+                    continue;
+                }
+                float yv[Cfg::D2], dyv[Cfg::D2];
+#pragma unroll
+                for (int i = 0; i < Cfg::D2; ++i) {
+                    yv[i] = IO<T>::load1(y + e * Cfg::D2 + i);
+                    dyv[i] = IO<T>::load1(ddy + e * Cfg::D2 + i);
+                }
+                sfor<Cfg::NP>([&](auto pp) {
+                    constexpr int p = decltype(pp)::value;
+                    constexpr PathInfo pi = Cfg::table.paths[p];
+                    if constexpr (pi.out_block == j) {
+                        constexpr int n1 = 2 * pi.l1 + 1;
+                        constexpr int na = Off<Cfg>::a[p + 1] - Off<Cfg>::a[p];
+                        float A[na], Ad[na];
+                        build_A<Cfg, p>(yv, A);
+                        build_A<Cfg, p>(dyv, Ad);
+                        float xr[n1][V], dr[n1][V], wv[V], dwv[V];
+#pragma unroll
+                        for (int m = 0; m < n1; ++m) {
+                            loadv<T, V>(x + (a * Cfg::D1 + pi.xoff + m) * Nq + c0, xr[m]);
+                            loadv<T, V>(ddx + (a * Cfg::D1 + pi.xoff + m) * Nq + c0, dr[m]);
+                        }
+                        loadv<T, V>(w + (e * Cfg::NP + p) * Nq + c0, wv);
+                        loadv<T, V>(ddw + (e * Cfg::NP + p) * Nq + c0, dwv);
+                        tp_rows_acc<Cfg, p, nrow, V>(A, dr, wv, acc, 0);    // TP(ddx, y, w)
+                        tp_rows_acc<Cfg, p, nrow, V>(Ad, xr, wv, acc, 0);   // TP(x, ddy, w)
+                        tp_rows_acc<Cfg, p, nrow, V>(A, xr, dwv, acc, 0);   // TP(x, y, ddw)
+                    }
+                });
+            }
+            constexpr int zo = Off<Cfg>::z[j];
+#pragma unroll
+            for (int i = 0; i < nrow; ++i) {
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[i][c] *= scale;
+                storev<V>(ddm + (b * Cfg::D + zo + i) * Nq + c0, acc[i]);
+            }
+        });
+    }
+}
+
+// one edge of the sender pass: accumulates delta_x into gxa, the lane's partial delta_y into
+// gyp and writes delta_w[e]
+template <class Cfg, class T, int V>
+__device__ __forceinline__ void dbackward_body(const T* __restrict__ x_a, const T* __restrict__ ddx_a,
+                                               const float (&yv)[Cfg::D2], const float (&dyv)[Cfg::D2],
+                                               const T* __restrict__ w_e, const T* __restrict__ ddw_e,
+                                               const T* __restrict__ g_row, float gscale, float* __restrict__ gw_e,
+                                               int Nq, int c0, float (&gxa)[Cfg::D1][V], float (&gyp)[Cfg::D2]) {
+    sfor<Cfg::NOUT>([&](auto jj) {
+        constexpr int j = decltype(jj)::value;
+        constexpr int nrow = 2 * Cfg::table.outs[j].l + 1;
+        constexpr int zo = Off<Cfg>::z[j];
+        float g[nrow][V];
+#pragma unroll
+        for (int m = 0; m < nrow; ++m) {
+            loadv<T, V>(g_row + (zo + m) * Nq + c0, g[m]);
+#pragma unroll
+            for (int c = 0; c < V; ++c) g[m][c] *= gscale;
+        }
+        sfor<Cfg::NP>([&](auto pp) {
+            constexpr int p = decltype(pp)::value;
+            constexpr PathInfo pi = Cfg::table.paths[p];
+            if constexpr (pi.out_block == j) {
+                constexpr int a0 = Off<Cfg>::a[p];
+                constexpr int na = Off<Cfg>::a[p + 1] - a0;
+                constexpr int n1 = 2 * pi.l1 + 1;
+                float A[na], Ad[na];
+                build_A<Cfg, p>(yv, A);
+                build_A<Cfg, p>(dyv, Ad);
+                float wv[V], dwv[V];
+                loadv<T, V>(w_e + p * Nq + c0, wv);
+                loadv<T, V>(ddw_e + p * Nq + c0, dwv);
+                float xr[n1][V], dr[n1][V], u[n1][V], gy[n1][V], gd[n1][V];
+#pragma unroll
+                for (int m = 0; m < n1; ++m) {
+                    loadv<T, V>(x_a + (pi.xoff + m) * Nq + c0, xr[m]);
+                    loadv<T, V>(ddx_a + (pi.xoff + m) * Nq + c0, dr[m]);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) {
+                        u[m][c] = fmaf(dr[m][c], wv[c], xr[m][c] * dwv[c]);
+                        gy[m][c] = 0.f;
+                        gd[m][c] = 0.f;
+                    }
+                }
+                sfor<na>([&](auto k) {
+                    constexpr AEnt e = Cfg::aents[a0 + decltype(k)::value];
+                    float s = 0.f;
+#pragma unroll
+                    for (int c = 0; c < V; ++c) {
+                        gy[e.m1][c] = fmaf(A[decltype(k)::value], g[e.m3][c], gy[e.m1][c]);
+                        gd[e.m1][c] = fmaf(Ad[decltype(k)::value], g[e.m3][c], gd[e.m1][c]);
+                        s = fmaf(u[e.m1][c], g[e.m3][c], s);
+                    }
+                    sfor<e.nt>([&](auto t) {
+                        constexpr int tt = decltype(t)::value;
+                        gyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, gyp[pi.yoff + e.m2[tt]]);
+                    });
+                });
+                float gwv[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int m = 0; m < n1; ++m) {
+                        s = fmaf(dr[m][c], gy[m][c], s);
+                        s = fmaf(xr[m][c], gd[m][c], s);
+                        gxa[pi.xoff + m][c] = fmaf(wv[c], gd[m][c], fmaf(dwv[c], gy[m][c], gxa[pi.xoff + m][c]));
+                    }
+                    gwv[c] = s;
+                }
+                storev<V>(gw_e + p * Nq + c0, gwv);
+            }
+        });
+    });
+}
+
+template <class Cfg, class T, int V>
+__global__ void __launch_bounds__(256) conv_dbwd_kernel(
+    int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
+    const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y, const T* __restrict__ w,
+    const T* __restrict__ dm, const T* __restrict__ ddx, const T* __restrict__ ddy, const T* __restrict__ ddw,
+    float scale, float* __restrict__ gx, float* __restrict__ gy, float* __restrict__ gw, int64_t pad,
+    unsigned* __restrict__ err) {
+    const Lanes L = lanes_for<V>(Nq);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int c0 = L.gl * V;
+    const int64_t iters = (N + nwarp * L.per_warp - 1) / (nwarp * L.per_warp);
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t a = (it * nwarp + warp) * L.per_warp + L.grp;
+        const bool live = a < N;
+        const int64_t aa = live ? a : 0;
+        float gxa[Cfg::D1][V];
+#pragma unroll
+        for (int i = 0; i < Cfg::D1; ++i)
+#pragma unroll
+            for (int c = 0; c < V; ++c) gxa[i][c] = 0.f;
+        int64_t k0 = 0, k1 = 0;
+        if (live) {
+            k0 = __ldg(csc_ptr + aa);
+            k1 = __ldg(csc_ptr + aa + 1);
+            if (k0 < 0 || k1 < k0 || k1 > E) {
+                if (L.gl == 0) atomicOr(err, kErrRowptr);
+                k0 = k1 = 0;
+            }
+            if (aa == pad) k0 = k1 = 0;
+        }
+        // the row groups of a warp may own different edge counts; loop to the warp maximum
+        int64_t cnt = k1 - k0, wmax = cnt;
+        for (int off = 16; off > 0; off >>= 1) {
+            const int64_t o = __shfl_xor_sync(0xffffffffu, wmax, off);
+            wmax = o > wmax ? o : wmax;
+        }
+        for (int64_t i = 0; i < wmax; ++i) {
+            bool ok = i < cnt;
+            int64_t e = 0, b = 0;
+            if (ok) {
+                e = __ldg(csc_edge + k0 + i);
+                b = __ldg(csc_recv + k0 + i);
+                if (pad >= 0 && b == pad) {
+                    ok = false;   // padding edge: its rows are zeroed separately
+                } else if (e < 0 || e >= E || b < 0 || b >= N) {
+                    if (L.gl == 0) atomicOr(err, kErrRecv);
+                    ok = false;
+                }
+            }
+            float gyp[Cfg::D2];
+#pragma unroll
+            for (int t = 0; t < Cfg::D2; ++t) gyp[t] = 0.f;
+            if (ok) {
+                float yv[Cfg::D2], dyv[Cfg::D2];
+#pragma unroll
+                for (int t = 0; t < Cfg::D2; ++t) {
+                    yv[t] = IO<T>::load1(y + e * Cfg::D2 + t);
+                    dyv[t] = IO<T>::load1(ddy + e * Cfg::D2 + t);
+                }
+                dbackward_body<Cfg, T, V>(x + aa * Cfg::D1 * Nq, ddx + aa * Cfg::D1 * Nq, yv, dyv,
+                                          w + e * Cfg::NP * Nq, ddw + e * Cfg::NP * Nq, dm + b * Cfg::D * Nq, scale,
+                                          gw + e * Cfg::NP * Nq, Nq, c0, gxa, gyp);
+            }
+            group_reduce<Cfg::D2>(gyp, L.G);
+            if (ok && L.gl == 0)
+#pragma unroll
+                for (int t = 0; t < Cfg::D2; ++t) gy[e * Cfg::D2 + t] = gyp[t];
+        }
+        if (live)
+#pragma unroll
+            for (int i = 0; i < Cfg::D1; ++i) storev<V>(gx + (aa * Cfg::D1 + i) * Nq + c0, gxa[i]);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
 // host-side launch table of one configuration
 // ------------------------------------------------------------------------------------------
 struct Launch {
@@ -536,6 +802,12 @@ struct ConfigOps {
     cudaError_t (*conv_bwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
                                const void*, const void*, const void*, const void*, float, void*, void*,
                                void*, int64_t, unsigned*, cudaStream_t);
+    // double backward: receiver CSR and sender-major index; x, y, w, dm, ddx, ddy, ddw in;
+    // delta_x, delta_y, delta_w, delta_dm out
+    cudaError_t (*conv_dbwd[2])(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                const int32_t*, const int32_t*, const void*, const void*, const void*,
+                                const void*, const void*, const void*, const void*, float, void*, void*, void*,
+                                void*, int64_t, unsigned*, cudaStream_t);
 };
 
 int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units);
