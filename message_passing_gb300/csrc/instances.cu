@@ -3,6 +3,7 @@
 // -DE3GB_PART=1 (backward kernels) and -DE3GB_PART=2 (double backward), so that the three
 // parts compile in parallel.
 #include "conv_pipe.cuh"
+#include "conv_pipe_dd.cuh"
 #include "kernels.cuh"
 
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
@@ -160,6 +161,31 @@ cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const
                       const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
                       const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
                       void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s) {
+    using SR = DdPipeShape<Cfg, T, false>;
+    using SS = DdPipeShape<Cfg, T, true>;
+    if constexpr (SR::usable && SS::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm) && aligned16(ddx) &&
+            aligned16(ddy) && aligned16(ddw)) {
+            auto kr = conv_ddm_pipe_kernel<Cfg, T, SR::NSLOT, SR::WARPS>;
+            auto ks = conv_dbwd_pipe_kernel<Cfg, T, SS::NSLOT, SS::WARPS>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)kr, cudaFuncAttributeMaxDynamicSharedMemorySize, SR::SMEM);
+            if (st == cudaSuccess)
+                st = cudaFuncSetAttribute((const void*)ks, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t nr = (N + SR::WARPS - 1) / SR::WARPS, ns = (N + SS::WARPS - 1) / SS::WARPS;
+            const int gr = int(sm_count() < nr ? sm_count() : nr), gs = int(sm_count() < ns ? sm_count() : ns);
+            if (gr == 0) return cudaSuccess;
+            kr<<<gr, SR::WARPS * 32, SR::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w,
+                                                     (const T*)ddx, (const T*)ddy, (const T*)ddw, scale, (float*)gdm,
+                                                     pad, err);
+            st = cudaGetLastError();
+            if (st != cudaSuccess) return st;
+            ks<<<gs, SS::WARPS * 32, SS::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
+                                                     (const T*)dm, (const T*)ddx, (const T*)ddy, (const T*)ddw, scale,
+                                                     (float*)gx, (float*)gy, (float*)gw, pad, err);
+            return cudaGetLastError();
+        }
+    }
     auto kr = vec_for(Nq) == 4 ? conv_ddm_kernel<Cfg, T, 4> : conv_ddm_kernel<Cfg, T, 1>;
     const int gr = grid_for((const void*)kr, kBlock, rows_per_block(Nq), N);
     if (gr == 0) return cudaSuccess;

@@ -112,9 +112,11 @@ def test_double_backward_equals_gpu_composition_and_is_deterministic():
     dx2, _, dw2 = e3.conv_backward(t, csc, x, ddy, w, dm, scale)
     dx3, dy3, _ = e3.conv_backward(t, csc, x, y, ddw, dm, scale)
     torch.cuda.synchronize()
+    # both sides are fp32 results each within TOL_F32 x RMS of the exact one, so they may
+    # differ by twice that
     for got, ref, name in ((a[0], dx2 + dx3, "delta_x"), (a[1], dy1 + dy3, "delta_y"), (a[2], dw1 + dw2, "delta_w"),
                            (a[3], ddm, "delta_dm")):
-        assert_close(to_np(got), to_np(ref), TOL_F32, name)
+        assert_close(to_np(got), to_np(ref), 2 * TOL_F32, name)
 
 
 def test_double_backward_padding():
