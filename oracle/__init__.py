@@ -25,6 +25,7 @@ import threading
 import numpy as np
 
 from .cg import cg_block
+from .coo import cg_records, coo_tp_backward, coo_tp_forward
 from .paths import Table, make_table
 from .sh import sh, sh_grad
 
@@ -266,6 +267,7 @@ def conv_double_backward(t: Table, rowptr, sender, x, y, w, dm, ddx, ddy, ddw, s
     return dx2 + dx3, dy1 + dy3, dw1 + dw2, ddm
 
 
-__all__ = ["sh", "sh_grad", "cg_block", "table", "tp_forward", "tp_backward", "conv_forward",
+__all__ = ["sh", "sh_grad", "cg_block", "cg_records", "coo_tp_forward", "coo_tp_backward", "table", "tp_forward",
+           "tp_backward", "conv_forward",
            "conv_backward_edges", "conv_backward_dx", "conv_double_backward", "build", "num_threads",
            "receivers_of"]
