@@ -226,9 +226,34 @@ e3gb_status e3gb_conv_double_backward(const e3gb_table *t, int64_t n_nodes, int6
                                       void *delta_w, void *delta_dm, e3gb_dtype dtype,
                                       void *stream);
 
+/* Tensor product with arbitrary sparse coefficients on rows (e3j App. E.1 Eq. (10)-(11),
+ * Alg. 1: C as a COO list of records), the general bilinear primitive of which the CG
+ * tensor product is one choice of records:
+ *   z[r,i0,q] = sum over records k with i0_k = i0 of coef[k] * w[r,path_k,q] * x[r,i1_k,q] * y[r,i2_k]
+ * rec: device int32 [n_rec][4] = (i0, i1, i2, path), 16-byte aligned, any order, repeats
+ * add; coef: device float [n_rec]. x [rows,d1,mul], y [rows,d2], w [rows,n_paths,mul]
+ * (dtype), z [rows,D,mul] fp32, fully overwritten (rows of z with no record are 0).
+ * mul: a power of two <= 128. E3GB_ERR_UNSUPPORTED when one block's accumulators do not fit
+ * in shared memory (forward: 1024 * D * (mul >= 64 ? 4 : 1) bytes). A record with an index
+ * outside D, d1, d2, n_paths is skipped and sets bit 8 of the device error word. Records
+ * and coefficients are caller-owned device memory; nothing is allocated. */
+e3gb_status e3gb_coo_tp_forward(int64_t rows, int32_t d1, int32_t d2, int32_t D, int32_t n_paths,
+                                int32_t mul, int32_t n_rec, const int32_t *rec, const float *coef,
+                                const void *x, const void *y, const void *w, void *z,
+                                e3gb_dtype dtype, void *stream);
+
+/* Its adjoint from dz [rows,D,mul]: dx [rows,d1,mul], dy [rows,d2], dw [rows,n_paths,mul],
+ * fp32, fully overwritten. Deterministic (fixed record order per row, fixed reduction of
+ * dy over channels). */
+e3gb_status e3gb_coo_tp_backward(int64_t rows, int32_t d1, int32_t d2, int32_t D, int32_t n_paths,
+                                 int32_t mul, int32_t n_rec, const int32_t *rec, const float *coef,
+                                 const void *x, const void *y, const void *w, const void *dz,
+                                 void *dx, void *dy, void *dw, e3gb_dtype dtype, void *stream);
+
 /* Synchronise stream, read and clear the device error word of the current device.
  * E3GB_OK when clean, E3GB_ERR_DEVICE_INDEX when a kernel skipped bad indices (*flags, if
- * not NULL, receives the bits: 1 bad sender, 2 bad CSR pointer, 4 bad receiver / edge id). */
+ * not NULL, receives the bits: 1 bad sender, 2 bad CSR pointer, 4 bad receiver / edge id,
+ * 8 bad COO record index). */
 e3gb_status e3gb_check_device_status(void *stream, int32_t *flags);
 
 /* Message of the last failed call on this thread ("" if none). */

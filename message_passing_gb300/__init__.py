@@ -28,7 +28,7 @@ SYMBOLS = (
     "e3gb_sh_backward",
     "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
     "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
-    "e3gb_conv_double_backward",
+    "e3gb_conv_double_backward", "e3gb_coo_tp_forward", "e3gb_coo_tp_backward",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
 )
 
@@ -77,6 +77,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_conv_backward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, f32, i64, vp, vp, vp, i32, vp]),
         "e3gb_conv_double_backward": (i32, [vp, i64, i64] + [vp] * 5 + [vp] * 7 + [f32, i64] + [vp] * 4
                                       + [i32, vp]),
+        "e3gb_coo_tp_forward": (i32, [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp]),
+        "e3gb_coo_tp_backward": (i32, [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                       vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
         "e3gb_last_error": (ctypes.c_char_p, []),
         "e3gb_version": (ctypes.c_char_p, []),
@@ -341,6 +344,38 @@ def conv_double_backward(t: Table, rowptr, sender, csc, x, y, w, dm, delta_dx, d
         _ptr(delta_dx), e(delta_dy), e(delta_dw), float(scale), int(pad_node), _ptr(gx), e(gy), e(gw), _ptr(gdm),
         _dtype(x, dm, delta_dx, *((y, w, delta_dy, delta_dw) if E else ())), _stream(stream)))
     return gx, gy, gw, gdm
+
+
+def coo_tp_forward(rec, coef, x, y, w, D: int, out=None, stream=None):
+    """Tensor product with runtime COO coefficients: rec int32 [n,4] (i0, i1, i2, path) and
+    coef fp32 [n] on the device; x [R,d1,mul], y [R,d2], w [R,P,mul] -> z [R,D,mul] fp32."""
+    import torch
+    _contig(rec, coef, x, y, w)
+    R, d1, mul = x.shape
+    z = out if out is not None else torch.empty((R, D, mul), dtype=torch.float32, device=x.device)
+    _f32_out(z)
+    n = rec.shape[0]
+    _check(load().e3gb_coo_tp_forward(R, d1, y.shape[1], D, w.shape[1], mul, n, _ptr(rec) if n else None,
+                                      _ptr(coef) if n else None, _ptr(x), _ptr(y), _ptr(w), _ptr(z), _dtype(x, y, w),
+                                      _stream(stream)))
+    return z
+
+
+def coo_tp_backward(rec, coef, x, y, w, dz, out=None, stream=None):
+    """(dx, dy, dw) of coo_tp_forward."""
+    import torch
+    _contig(rec, coef, x, y, w, dz)
+    R, d1, mul = x.shape
+    if out is None:
+        f = dict(dtype=torch.float32)
+        out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f))
+    dx, dy, dw = out
+    _f32_out(dx, dy, dw)
+    n = rec.shape[0]
+    _check(load().e3gb_coo_tp_backward(R, d1, y.shape[1], dz.shape[1], w.shape[1], mul, n, _ptr(rec) if n else None,
+                                       _ptr(coef) if n else None, _ptr(x), _ptr(y), _ptr(w), _ptr(dz), _ptr(dx),
+                                       _ptr(dy), _ptr(dw), _dtype(x, y, w, dz), _stream(stream)))
+    return dx, dy, dw
 
 
 def check_device_status(stream=None) -> int:

@@ -56,7 +56,7 @@ def _stale(obj: str, deps: list[str]) -> bool:
 def units() -> list[tuple[str, str, list[str]]]:
     """(source, object, extra flags)"""
     u = [(os.path.join(CSRC, s), os.path.join(OBJDIR, s.replace(".cu", ".o")), [])
-         for s in ("api.cu", "sh.cu", "graph.cu")]
+         for s in ("api.cu", "sh.cu", "graph.cu", "coo.cu")]
     for i in config_ids():
         for part in (0, 1, 2):   # forward, backward, double backward
             u.append((os.path.join(CSRC, "instances.cu"), os.path.join(OBJDIR, f"cfg{i}_{part}.o"),

@@ -31,6 +31,11 @@ cudaError_t sh_backward(int lmax, int64_t n, const float* vec, const void* dy, f
 size_t graph_workspace_bytes(int64_t N);
 cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
                           int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s);
+size_t coo_smem_bytes(bool backward, int d1, int d2, int D, int P, int Nq);
+template <class T>
+cudaError_t coo_tp(bool backward, int64_t R, int d1, int d2, int D, int P, int Nq, int nrec, const int32_t* rec,
+                   const float* coef, const void* x, const void* y, const void* w, const void* dz, void* z_or_dx,
+                   void* dy, void* dw, unsigned* err, cudaStream_t s);
 cudaError_t zero_padding_edges(int64_t N, int64_t E, const int32_t* csc_ptr, const int32_t* csc_edge,
                                const int32_t* csc_recv, int64_t pad, float* dw, int64_t dw_row, float* dy,
                                int64_t dy_row, cudaStream_t s);
@@ -490,6 +495,60 @@ e3gb_status e3gb_conv_double_backward(const e3gb_table* t, int64_t n_nodes, int6
                                           int64_t(t->ops->NP) * t->mul, (float*)delta_y, t->ops->D2,
                                           (cudaStream_t)stream),
                        "zero_padding_edges launch");
+}
+
+namespace {
+e3gb_status coo_common(bool backward, int64_t rows, int32_t d1, int32_t d2, int32_t D, int32_t n_paths, int32_t mul,
+                       int32_t n_rec, const int32_t* rec, const float* coef, const void* x, const void* y,
+                       const void* w, const void* dz, void* out0, void* out1, void* out2, e3gb_dtype dtype,
+                       void* stream) {
+    if (dtype != E3GB_F32 && dtype != E3GB_BF16) return fail(E3GB_ERR_INVALID_ARG, "unknown dtype");
+    if (rows < 0 || n_rec < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (d1 < 1 || d2 < 1 || D < 1 || n_paths < 1) return fail(E3GB_ERR_INVALID_ARG, "d1, d2, D, n_paths must be >= 1");
+    if (!(mul == 1 || mul == 2 || mul == 4 || mul == 8 || mul == 16 || mul == 32 || mul == 64 || mul == 128))
+        return fail(E3GB_ERR_UNSUPPORTED, "mul %d not a power of two <= 128", mul);
+    if (coo_smem_bytes(backward, d1, d2, D, n_paths, mul) > 232448)
+        return fail(E3GB_ERR_UNSUPPORTED, "output rows x channels too large for one block's shared memory");
+    if (rows == 0) return ok();
+    const size_t va = mul >= 64 ? vec_align(dtype) : elt_bytes(dtype), ea = elt_bytes(dtype);
+    E3GB_TRY(check_ptr(rec, "records", 16, n_rec > 0));
+    E3GB_TRY(check_ptr(coef, "coefficients", 4, n_rec > 0));
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, true));
+    E3GB_TRY(check_ptr(w, "w", va, true));
+    if (backward) {
+        E3GB_TRY(check_ptr(dz, "dz", va, true));
+        E3GB_TRY(check_ptr(out0, "dx", mul >= 64 ? 16 : 4, true));
+        E3GB_TRY(check_ptr(out1, "dy", 4, true));
+        E3GB_TRY(check_ptr(out2, "dw", mul >= 64 ? 16 : 4, true));
+    } else {
+        E3GB_TRY(check_ptr(out0, "z", mul >= 64 ? 16 : 4, true));
+    }
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    const cudaError_t e =
+        dtype == E3GB_F32
+            ? coo_tp<float>(backward, rows, d1, d2, D, n_paths, mul, n_rec, rec, coef, x, y, w, dz, out0, out1, out2,
+                            err, (cudaStream_t)stream)
+            : coo_tp<__nv_bfloat16>(backward, rows, d1, d2, D, n_paths, mul, n_rec, rec, coef, x, y, w, dz, out0,
+                                    out1, out2, err, (cudaStream_t)stream);
+    return cuda_status(e, backward ? "coo_tp_backward launch" : "coo_tp_forward launch");
+}
+}  // namespace
+
+e3gb_status e3gb_coo_tp_forward(int64_t rows, int32_t d1, int32_t d2, int32_t D, int32_t n_paths, int32_t mul,
+                                int32_t n_rec, const int32_t* rec, const float* coef, const void* x, const void* y,
+                                const void* w, void* z, e3gb_dtype dtype, void* stream) {
+    return coo_common(false, rows, d1, d2, D, n_paths, mul, n_rec, rec, coef, x, y, w, nullptr, z, nullptr, nullptr,
+                      dtype, stream);
+}
+
+e3gb_status e3gb_coo_tp_backward(int64_t rows, int32_t d1, int32_t d2, int32_t D, int32_t n_paths, int32_t mul,
+                                 int32_t n_rec, const int32_t* rec, const float* coef, const void* x, const void* y,
+                                 const void* w, const void* dz, void* dx, void* dy, void* dw, e3gb_dtype dtype,
+                                 void* stream) {
+    return coo_common(true, rows, d1, d2, D, n_paths, mul, n_rec, rec, coef, x, y, w, dz, dx, dy, dw, dtype, stream);
 }
 
 e3gb_status e3gb_check_device_status(void* stream, int32_t* flags) {

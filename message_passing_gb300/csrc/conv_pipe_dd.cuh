@@ -299,10 +299,9 @@ __device__ __forceinline__ void dbwd_block(const unsigned char* __restrict__ slo
                     constexpr AEnt e = Cfg::aents[a0 + kk];
                     gy[e.m1] = q2_fma(ay[decltype(cc)::value], g[e.m3], gy[e.m1]);
                     gd[e.m1] = q2_fma(ad[decltype(cc)::value], g[e.m3], gd[e.m1]);
-                    float s = u[e.m1].lo.x * g[e.m3].lo.x;
-                    s = fmaf(u[e.m1].lo.y, g[e.m3].lo.y, s);
-                    s = fmaf(u[e.m1].hi.x, g[e.m3].hi.x, s);
-                    s = fmaf(u[e.m1].hi.y, g[e.m3].hi.y, s);
+                    // sum over the lane's 4 channels of (ddx w + x ddw) g, for delta_y
+                    const float2 s2 = __ffma2_rn(u[e.m1].hi, g[e.m3].hi, __fmul2_rn(u[e.m1].lo, g[e.m3].lo));
+                    const float s = s2.x + s2.y;
                     sfor<e.nt>([&](auto t) {
                         constexpr int tt = decltype(t)::value;
                         dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
@@ -477,7 +476,10 @@ conv_dbwd_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr, co
 
 template <class Cfg, class T, bool SENDER>
 struct DdPipeShape {
-    static constexpr int NSLOT = SENDER ? 3 : 4;
+    // 2 slots for the sender pass (its items are 15 rows) and 3 for the receiver pass give
+    // 8 warps per SM; measured on the 64k-atom workload: sender 3 -> 2 slots 69.4 -> 58.1 ms,
+    // receiver 4 -> 3 slots a further ~2 ms
+    static constexpr int NSLOT = SENDER ? 2 : 3;
     static constexpr int WARP_BYTES =
         SENDER ? DbwdPipe<Cfg, T, NSLOT>::WARP_BYTES : DdmPipe<Cfg, T, NSLOT>::WARP_BYTES;
     static constexpr int by_smem = kSmemLimit / WARP_BYTES;
