@@ -364,6 +364,47 @@ def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float):
     return res
 
 
+def time_coo_tp(wl, dev, stream, reps: int, hbm_peak: float):
+    """The generic COO-coefficient tensor product with the table's CG records, beside the
+    compile-time kernels, on a row workload (fp32)."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import workloads as W
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    rec, coef = t.coo_records()
+    rec_d, coef_d = torch.from_numpy(rec).to(dev), torch.from_numpy(coef).to(dev)
+    u, x, ww = W.make_tp(wl, t.n_paths)
+    R = x.shape[0]
+    xd, wd = torch.from_numpy(x).to(dev), torch.from_numpy(ww).to(dev)
+    y = e3.sh_forward(torch.from_numpy(u.astype(np.float32)).to(dev), wl.sh_lmax)
+    dz = torch.from_numpy(W.make_grad(wl, R, t.D)).to(dev)
+    z = torch.empty((R, t.D, wl.mul), device=dev)
+    gx, gy, gw = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(wd)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        ev[k][0].record(stream)
+        e3.coo_tp_forward(rec_d, coef_d, xd, y, wd, t.D, out=z, stream=stream)
+        ev[k][1].record(stream)
+        e3.coo_tp_backward(rec_d, coef_d, xd, y, wd, dz, out=(gx, gy, gw), stream=stream)
+        ev[k][2].record(stream)
+        e3.tp_forward(t, xd, y, wd, out=z, stream=stream)
+        ev[k][3].record(stream)
+        e3.tp_backward(t, xd, y, wd, dz, out=(gx, gy, gw), stream=stream)
+        ev[k][4].record(stream)
+    torch.cuda.synchronize()
+    e3.check_device_status()
+    tms = [_median([e[i].elapsed_time(e[i + 1]) for e in ev[2:]]) / 1e3 for i in range(4)]
+    bf, bb = tp_bytes(R, t.d1, t.d2, t.n_paths, t.D, wl.mul, 4)
+    res = {"workload": wl.name + " (generic COO records)", "dtype": "f32", "rows": R, "records": int(len(rec)),
+           "fwd": {"ms": tms[0] * 1e3, "alg_GBps": bf / tms[0] / 1e9, "frac": bf / tms[0] / 1e9 / hbm_peak},
+           "bwd": {"ms": tms[1] * 1e3, "alg_GBps": bb / tms[1] / 1e9, "frac": bb / tms[1] / 1e9 / hbm_peak},
+           "compile_time_tables": {"fwd_ms": tms[2] * 1e3, "bwd_ms": tms[3] * 1e3}}
+    del xd, wd, y, dz, z, gx, gy, gw
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_tp_workload(wl, dev, stream, reps: int, hbm_peak: float):
     """Per-kernel device times of TP forward and backward on a row workload (fp32)."""
     import torch
@@ -595,6 +636,7 @@ def run_ours(args):
                   time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak),
                   time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak, pad_frac=0.25)]
         double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak)
+        others.append(time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak))
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None

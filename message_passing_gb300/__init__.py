@@ -191,6 +191,20 @@ class Table:
         _check(load().e3gb_table_coefficients(self.handle, buf))
         return np.frombuffer(buf, dtype=np.float64).reshape(self.nnz, 5).copy()
 
+    def coo_records(self):
+        """The table's CG tensor product as records for coo_tp_forward: (int32 [n,4] rows
+        (i0, i1, i2, path), float32 [n] coefficients), host arrays."""
+        import numpy as np
+        xoff = np.concatenate([[0], np.cumsum([2 * l + 1 for l, _ in self.blocks])])
+        paths = np.array(self.paths(), dtype=np.int64).reshape(-1, 8)
+        co = self.coefficients()
+        p = co[:, 0].astype(np.int64)
+        rec = np.stack([paths[p, 7] + co[:, 3].astype(np.int64),            # output offset + m3
+                        xoff[paths[p, 0]] + co[:, 1].astype(np.int64),      # x block offset + m1
+                        paths[p, 3] ** 2 + co[:, 2].astype(np.int64),       # l2^2 + m2
+                        p], axis=1).astype(np.int32)
+        return np.ascontiguousarray(rec), co[:, 4].astype(np.float32)
+
     def __del__(self):
         h = getattr(self, "handle", None)
         if h is not None and h.value and _lib is not None:

@@ -100,3 +100,18 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.e3gb_sh_forward(4, 3, None, None, 0, None) == e3.ERR_UNSUPPORTED
     assert lib.e3gb_graph_prepare(10, 20, None, None, None, None, None, None, 0, None) == e3.ERR_INVALID_ARG
     assert lib.e3gb_graph_prepare_workspace_bytes(1000) >= 1001 * 4
+
+
+def test_table_coo_records_match_the_oracle_records():
+    """The binding's CG records (library table, host side) are the oracle's CG records up to
+    order and rounding to fp32."""
+    import numpy as np
+    import oracle
+    blocks = [(0, 1), (1, -1), (2, 1)]
+    t = e3.Table.create(blocks, 128, 3, 3)
+    rec, c = t.coo_records()
+    orec, oc = oracle.cg_records(oracle.table(blocks, 3, 3))
+    key = lambda r: np.lexsort(r.T[::-1])
+    a, b = key(rec), key(orec)
+    assert np.array_equal(rec[a], orec[b])
+    np.testing.assert_allclose(c[a], oc[b], rtol=1e-6, atol=1e-7)
