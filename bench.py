@@ -313,7 +313,7 @@ def dbwd_bytes(N, E, d1, d2, P, D, Nq, s):
             + (N * d1 * Nq + E * d2 + E * P * Nq + N * D * Nq) * 4)
 
 
-def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float):
+def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None):
     """Device time of the fused double backward (Eq. 17-18) on a conv workload, and of the
     pages' formulation beside it: three conv and three conv_bwd calls (their three output
     additions not counted)."""
@@ -323,7 +323,7 @@ def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float):
     from synth import STREAM_GRAD, STREAM_W, device_normal
     from synth import workloads as W
     t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
-    g = W.make_graph(wl)
+    g = W.make_graph(wl, n_atoms=n_atoms)
     N, E, Nq, P, D = g.n_nodes, g.n_edges, wl.mul, t.n_paths, t.D
     scale = N / E
     x_np, _ = W.make_conv(wl, g, P, edge_ids=np.zeros(0, np.int64))
@@ -629,14 +629,18 @@ def run_ours(args):
     if rank == 0 and not args.no_workloads:
         del wd, dmd, dx, dy, dw, xd, y, m
         torch.cuda.empty_cache()
-        others = [time_tp_workload(W.WORKLOADS[1], dev, stream, 20, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak),
-                  time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak, pad_frac=0.25)]
-        double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak)
-        others.append(time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak))
+        want = set(args.workloads.split(","))
+        jobs = [("tp1", lambda: time_tp_workload(W.WORKLOADS[1], dev, stream, 20, hbm_peak)),
+                ("conv4", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak)),
+                ("conv3", lambda: time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak)),
+                ("conv4bf16", lambda: time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak)),
+                ("conv5", lambda: time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak)),
+                ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
+                                                   pad_frac=0.25)),
+                ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak))]
+        others = [f() for k, f in jobs if "all" in want or k in want]
+        if "all" in want or "dbwd" in want:
+            double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak, n_atoms=args.dbwd_atoms)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -686,6 +690,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload kernel timings")
+    ap.add_argument("--workloads", default="all",
+                    help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,dbwd (or all)")
+    ap.add_argument("--dbwd-atoms", type=int, default=None, help="smaller double-backward case (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
