@@ -1,13 +1,14 @@
-// One irreps configuration's kernels and launchers; compiled three times per entry of configs.def,
+// One irreps configuration's kernels and launchers; compiled four times per entry of configs.def,
 // with -DE3GB_CFG=<id> -DE3GB_PART=0 (forward kernels and the ops table e3gb::ops_<id>())
-// -DE3GB_PART=1 (backward kernels) and -DE3GB_PART=2 (double backward), so that the three
-// parts compile in parallel.
+// -DE3GB_PART=1 (backward kernels), -DE3GB_PART=2 (double backward, plain kernels) and
+// -DE3GB_PART=3 (double backward, 128-channel pipelined kernels), so that the parts compile
+// in parallel.
 #include "conv_pipe.cuh"
 #include "conv_pipe_dd.cuh"
 #include "kernels.cuh"
 
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
-#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2>"
+#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3>"
 #endif
 #define E3GB_CAT2(a, b) a##b
 #define E3GB_CAT(a, b) E3GB_CAT2(a, b)
@@ -61,6 +62,12 @@ cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const
                       const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
                       const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
                       void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s);
+// the pipelined double backward (part 3); returns false when the shape needs the plain kernels
+template <class T>
+bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
+                    const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
+                    const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx, void* gy,
+                    void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s, cudaError_t* st);
 
 #if E3GB_PART == 0
 template <class T>
@@ -161,31 +168,10 @@ cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const
                       const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
                       const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
                       void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s) {
-    using SR = DdPipeShape<Cfg, T, false>;
-    using SS = DdPipeShape<Cfg, T, true>;
-    if constexpr (SR::usable && SS::usable) {
-        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm) && aligned16(ddx) &&
-            aligned16(ddy) && aligned16(ddw)) {
-            auto kr = conv_ddm_pipe_kernel<Cfg, T, SR::NSLOT, SR::WARPS>;
-            auto ks = conv_dbwd_pipe_kernel<Cfg, T, SS::NSLOT, SS::WARPS>;
-            cudaError_t st = cudaFuncSetAttribute((const void*)kr, cudaFuncAttributeMaxDynamicSharedMemorySize, SR::SMEM);
-            if (st == cudaSuccess)
-                st = cudaFuncSetAttribute((const void*)ks, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::SMEM);
-            if (st != cudaSuccess) return st;
-            const int64_t nr = (N + SR::WARPS - 1) / SR::WARPS, ns = (N + SS::WARPS - 1) / SS::WARPS;
-            const int gr = int(sm_count() < nr ? sm_count() : nr), gs = int(sm_count() < ns ? sm_count() : ns);
-            if (gr == 0) return cudaSuccess;
-            kr<<<gr, SR::WARPS * 32, SR::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w,
-                                                     (const T*)ddx, (const T*)ddy, (const T*)ddw, scale, (float*)gdm,
-                                                     pad, err);
-            st = cudaGetLastError();
-            if (st != cudaSuccess) return st;
-            ks<<<gs, SS::WARPS * 32, SS::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                                                     (const T*)dm, (const T*)ddx, (const T*)ddy, (const T*)ddw, scale,
-                                                     (float*)gx, (float*)gy, (float*)gw, pad, err);
-            return cudaGetLastError();
-        }
-    }
+    cudaError_t pst = cudaSuccess;
+    if (conv_dbwd_pipe<T>(N, E, Nq, rowptr, sender, cptr, cedge, crecv, x, y, w, dm, ddx, ddy, ddw, scale, gx, gy,
+                          gw, gdm, pad, err, s, &pst))
+        return pst;
     auto kr = vec_for(Nq) == 4 ? conv_ddm_kernel<Cfg, T, 4> : conv_ddm_kernel<Cfg, T, 1>;
     const int gr = grid_for((const void*)kr, kBlock, rows_per_block(Nq), N);
     if (gr == 0) return cudaSuccess;
@@ -210,6 +196,50 @@ template cudaError_t conv_dbwd<__nv_bfloat16>(int64_t, int64_t, int, const int32
                                                const void*, const void*, const void*, const void*, float, void*,
                                                void*, void*, void*, int64_t, unsigned*, cudaStream_t);
 #endif  // part 2
+#if E3GB_PART == 3
+template <class T>
+bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
+                    const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
+                    const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx, void* gy,
+                    void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s, cudaError_t* st) {
+    using SR = DdPipeShape<Cfg, T, false>;
+    using SS = DdPipeShape<Cfg, T, true>;
+    if constexpr (SR::usable && SS::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm) && aligned16(ddx) &&
+            aligned16(ddy) && aligned16(ddw)) {
+            auto kr = conv_ddm_pipe_kernel<Cfg, T, SR::NSLOT, SR::WARPS>;
+            auto ks = conv_dbwd_pipe_kernel<Cfg, T, SS::NSLOT, SS::WARPS>;
+            cudaError_t e = cudaFuncSetAttribute((const void*)kr, cudaFuncAttributeMaxDynamicSharedMemorySize, SR::SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute((const void*)ks, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::SMEM);
+            if (e != cudaSuccess) { *st = e; return true; }
+            const int64_t nr = (N + SR::WARPS - 1) / SR::WARPS, ns = (N + SS::WARPS - 1) / SS::WARPS;
+            const int gr = int(sm_count() < nr ? sm_count() : nr), gs = int(sm_count() < ns ? sm_count() : ns);
+            if (gr == 0) { *st = cudaSuccess; return true; }
+            kr<<<gr, SR::WARPS * 32, SR::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w,
+                                                     (const T*)ddx, (const T*)ddy, (const T*)ddw, scale, (float*)gdm,
+                                                     pad, err);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) { *st = e; return true; }
+            ks<<<gs, SS::WARPS * 32, SS::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
+                                                     (const T*)dm, (const T*)ddx, (const T*)ddy, (const T*)ddw, scale,
+                                                     (float*)gx, (float*)gy, (float*)gw, pad, err);
+            *st = cudaGetLastError();
+            return true;
+        }
+    }
+    return false;
+}
+
+template bool conv_dbwd_pipe<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                     const int32_t*, const int32_t*, const void*, const void*, const void*, const void*,
+                                     const void*, const void*, const void*, float, void*, void*, void*, void*, int64_t,
+                                     unsigned*, cudaStream_t, cudaError_t*);
+template bool conv_dbwd_pipe<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                             const int32_t*, const int32_t*, const void*, const void*, const void*,
+                                             const void*, const void*, const void*, const void*, float, void*, void*,
+                                             void*, void*, int64_t, unsigned*, cudaStream_t, cudaError_t*);
+#endif  // part 3
 }  // namespace cfg<id>
 
 #if E3GB_PART == 0
