@@ -41,6 +41,24 @@ template <>
 __device__ __forceinline__ void cp_async_slice<__nv_bfloat16>(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// L2 policy for operands read exactly once (the edge weights): their lines go first when L2
+// needs room, which keeps the gathered node rows (x, dm) resident longer
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// cp_async_slice with an L2 cache policy
+template <class T>
+__device__ __forceinline__ void cp_async_slice_hint(void* dst, const void* src, uint64_t pol);
+template <>
+__device__ __forceinline__ void cp_async_slice_hint<float>(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "l"(pol) : "memory");
+}
+template <>
+__device__ __forceinline__ void cp_async_slice_hint<__nv_bfloat16>(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -295,6 +313,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
     const int64_t nw = int64_t(gridDim.x) * WARPS;
+    const uint64_t wpol = l2_policy_evict_first();
 
     // producer cursor: next item to issue = (edge pe of node pn, chunk pc)
     int64_t pn = gw, pe = 0, pend = 0;
@@ -332,7 +351,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
                 const T* src = w + (pe * Cfg::NP + p0) * kPipeNq + c0;
 #pragma unroll
                 for (int r = 0; r < PP::PPC; ++r)
-                    if (r < np) cp_async_slice<T>(slot + r * F::ROWB + c0 * sizeof(T), src + r * kPipeNq);
+                    if (r < np) cp_async_slice_hint<T>(slot + r * F::ROWB + c0 * sizeof(T), src + r * kPipeNq, wpol);
             }
             if (++pc == F::NCH) {
                 pc = 0;
@@ -454,11 +473,9 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
                 if constexpr (kk < na) {
                     constexpr AEnt e = Cfg::aents[a0 + kk];
                     gp[e.m1] = q2_fma(av[decltype(cc)::value], g[e.m3], gp[e.m1]);
-                    // sum over the lane's 4 channels of x w g, for dy (scalar: 4 pipe cycles)
-                    float s = xw[e.m1].lo.x * g[e.m3].lo.x;
-                    s = fmaf(xw[e.m1].lo.y, g[e.m3].lo.y, s);
-                    s = fmaf(xw[e.m1].hi.x, g[e.m3].hi.x, s);
-                    s = fmaf(xw[e.m1].hi.y, g[e.m3].hi.y, s);
+                    // sum over the lane's 4 channels of x w g, for dy (two paired products, one add)
+                    const float2 s2 = __ffma2_rn(xw[e.m1].hi, g[e.m3].hi, __fmul2_rn(xw[e.m1].lo, g[e.m3].lo));
+                    const float s = s2.x + s2.y;
                     sfor<e.nt>([&](auto t) {
                         constexpr int tt = decltype(t)::value;
                         dyp[pi.yoff + e.m2[tt]] = fmaf(e.c[tt], s, dyp[pi.yoff + e.m2[tt]]);
@@ -476,7 +493,10 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
     });
 }
 
-template <class Cfg, class T, int NSLOT, int WARPS>
+// IDENT: the identity graph of the row-wise tensor product backward (App. E.1 Eq. (15)): row r
+// is a node with the single edge r from and to itself, scale 1; the index arrays are not read
+// and may be null, and so may err (no index can be out of range).
+template <class Cfg, class T, int NSLOT, int WARPS, bool IDENT = false>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr, const int32_t* __restrict__ cedge,
                           const int32_t* __restrict__ crecv, const T* __restrict__ x, const T* __restrict__ y,
@@ -493,6 +513,22 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
     const int64_t nw = int64_t(gridDim.x) * WARPS;
+    const uint64_t wpol = l2_policy_evict_first();
+    auto cp_at = [&](int64_t i) -> int64_t {
+        if constexpr (IDENT) return i;
+        else return __ldg(cptr + i);
+    };
+    auto ce_at = [&](int64_t k) -> int64_t {
+        if constexpr (IDENT) return k;
+        else return __ldg(cedge + k);
+    };
+    auto cr_at = [&](int64_t k) -> int64_t {
+        if constexpr (IDENT) return k;
+        else return __ldg(crecv + k);
+    };
+    auto flag = [&](unsigned bits) {
+        if constexpr (!IDENT) atomicOr(err, bits);
+    };
 
     // producer cursor: sender pa, edge position pk in [pk, pkend), item pc (-1: x rows of pa)
     int64_t pa = gw - nw, pk = 0, pkend = 0;
@@ -503,12 +539,12 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
     // padding receiver one by one
     auto p_skip_pad = [&]() {
         if (pad >= 0)
-            while (pk < pkend && __ldg(crecv + pk) == pad) ++pk;
+            while (pk < pkend && cr_at(pk) == pad) ++pk;
     };
     auto p_next_sender = [&]() {
         pa += nw;
         if (pa >= N) { pdone = true; return; }
-        int64_t k0 = __ldg(cptr + pa), k1 = __ldg(cptr + pa + 1);
+        int64_t k0 = cp_at(pa), k1 = cp_at(pa + 1);
         if (!seg_ok(k0, k1, E) || pa == pad) k0 = k1 = 0;
         pk = k0;
         pkend = k1;
@@ -525,7 +561,7 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                 pc = 0;
                 if (pk >= pkend) p_next_sender();
             } else {
-                const int64_t e = __ldg(cedge + pk), bb = __ldg(crecv + pk);
+                const int64_t e = ce_at(pk), bb = cr_at(pk);
                 const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
                 if (ok) {
                     // rows of output block pc: dm rows, then w rows of its paths; y behind them
@@ -540,8 +576,8 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                                                   dm + (bb * Cfg::D + zo + r) * kPipeNq + c0);
                             sfor<PP::bpos[j + 1] - PP::bpos[j]>([&](auto ii) {
                                 constexpr int p = PP::bpath[PP::bpos[j] + decltype(ii)::value];
-                                cp_async_slice<T>(slot + (nrow + decltype(ii)::value) * B::ROWB + c0 * sizeof(T),
-                                                  w + (e * Cfg::NP + p) * kPipeNq + c0);
+                                cp_async_slice_hint<T>(slot + (nrow + decltype(ii)::value) * B::ROWB + c0 * sizeof(T),
+                                                  w + (e * Cfg::NP + p) * kPipeNq + c0, wpol);
                             });
                         }
                     });
@@ -565,9 +601,9 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
 
     int64_t item = 0;
     for (int64_t a = gw; a < N; a += nw) {
-        int64_t k0 = __ldg(cptr + a), k1 = __ldg(cptr + a + 1);
+        int64_t k0 = cp_at(a), k1 = cp_at(a + 1);
         if (!seg_ok(k0, k1, E)) {
-            if (lane == 0) atomicOr(err, kErrRowptr);
+            if (lane == 0) flag(kErrRowptr);
             k0 = k1 = 0;
         }
         if (a == pad) k0 = k1 = 0;
@@ -585,10 +621,10 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
             }
         }
         for (int64_t k = k0; k < k1; ++k) {
-            const int64_t e = __ldg(cedge + k), bb = __ldg(crecv + k);
+            const int64_t e = ce_at(k), bb = cr_at(k);
             if (pad >= 0 && bb == pad) continue;   // not issued by the producer either
             const bool ok = e >= 0 && e < E && bb >= 0 && bb < N;
-            if (!ok && lane == 0) atomicOr(err, kErrRecv);
+            if (!ok && lane == 0) flag(kErrRecv);
             float dyp[Cfg::D2];
 #pragma unroll
             for (int t = 0; t < Cfg::D2; ++t) dyp[t] = 0.f;

@@ -1,14 +1,15 @@
-// One irreps configuration's kernels and launchers; compiled four times per entry of configs.def,
+// One irreps configuration's kernels and launchers; compiled five times per entry of configs.def,
 // with -DE3GB_CFG=<id> -DE3GB_PART=0 (forward kernels and the ops table e3gb::ops_<id>())
-// -DE3GB_PART=1 (backward kernels), -DE3GB_PART=2 (double backward, plain kernels) and
-// -DE3GB_PART=3 (double backward, 128-channel pipelined kernels), so that the parts compile
-// in parallel.
+// -DE3GB_PART=1 (backward kernels), -DE3GB_PART=2 (double backward, plain kernels),
+// -DE3GB_PART=3 (double backward, 128-channel pipelined kernels) and -DE3GB_PART=4 (forward,
+// edge-slot kernels for 4-32 channels), so that the parts compile in parallel.
 #include "conv_pipe.cuh"
 #include "conv_pipe_dd.cuh"
+#include "conv_slots.cuh"
 #include "kernels.cuh"
 
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
-#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3>"
+#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3|4>"
 #endif
 #define E3GB_CAT2(a, b) a##b
 #define E3GB_CAT(a, b) E3GB_CAT2(a, b)
@@ -62,6 +63,12 @@ cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const
                       const int32_t* cedge, const int32_t* crecv, const void* x, const void* y, const void* w,
                       const void* dm, const void* ddx, const void* ddy, const void* ddw, float scale, void* gx,
                       void* gy, void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s);
+// the edge-slot forward for 4-32 channels (part 4); returns false when the shape needs the
+// plain kernels
+template <class T>
+bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, cudaStream_t s,
+                    cudaError_t* st);
 // the pipelined double backward (part 3); returns false when the shape needs the plain kernels
 template <class T>
 bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
@@ -85,6 +92,23 @@ cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* 
 template <class T>
 cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* w, const void* dz, void* dx,
                    void* dy, void* dw, cudaStream_t s) {
+    using S = PipeShape<Cfg, T, true>;
+    if constexpr (S::usable) {
+        // 128 channels: the pipelined convolution backward on the identity graph (row r is node
+        // r with the one edge r), which streams the rows through the per-warp cp.async ring
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dz)) {
+            auto k = conv_backward_pipe_kernel<Cfg, T, S::NSLOT, S::WARPS, true>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t need = (R + S::WARPS - 1) / S::WARPS;
+            const int grid = int(sm_count() < need ? sm_count() : need);
+            if (grid == 0) return cudaSuccess;
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(R, R, nullptr, nullptr, nullptr, (const T*)x, (const T*)y,
+                                                   (const T*)w, (const T*)dz, 1.f, (float*)dx, (float*)dy, (float*)dw,
+                                                   -1, nullptr);
+            return cudaGetLastError();
+        }
+    }
     auto k = vec_for(Nq) == 4 ? tp_backward_kernel<Cfg, T, 4> : tp_backward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
     if (grid == 0) return cudaSuccess;
@@ -114,6 +138,8 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
             return cudaGetLastError();
         }
     }
+    cudaError_t sst = cudaSuccess;
+    if (conv_fwd_slots<T>(N, E, Nq, rowptr, sender, x, y, w, scale, m, pad, err, s, &sst)) return sst;
     auto k = vec_for(Nq) == 4 ? conv_forward_kernel<Cfg, T, 4> : conv_forward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
@@ -123,6 +149,43 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
 }
 
 #endif  // part 0
+
+#if E3GB_PART == 4
+template <class T, int NQ>
+static cudaError_t launch_fwd_slots(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, const void* x,
+                                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                                    cudaStream_t s) {
+    auto k = conv_forward_slots_kernel<Cfg, T, NQ>;
+    const int grid = grid_for((const void*)k, kBlock, slots_nodes_per_block<NQ>(), N);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, 0, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m, pad, err);
+    return cudaGetLastError();
+}
+
+template <class T>
+bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, cudaStream_t s,
+                    cudaError_t* st) {
+    if constexpr (SlotsFit<Cfg>::value) {
+        if (aligned16(x) && aligned16(y) && aligned16(w) && aligned16(m)) {
+            switch (Nq) {
+            case 4: *st = launch_fwd_slots<T, 4>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
+            case 8: *st = launch_fwd_slots<T, 8>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
+            case 16: *st = launch_fwd_slots<T, 16>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
+            case 32: *st = launch_fwd_slots<T, 32>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
+            default: break;
+            }
+        }
+    }
+    return false;
+}
+
+template bool conv_fwd_slots<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*, const void*,
+                                     const void*, float, void*, int64_t, unsigned*, cudaStream_t, cudaError_t*);
+template bool conv_fwd_slots<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
+                                             const void*, const void*, float, void*, int64_t, unsigned*, cudaStream_t,
+                                             cudaError_t*);
+#endif  // part 4
 
 #if E3GB_PART == 1
 template <class T>
