@@ -128,6 +128,16 @@ def test_determinism_bitwise():
         again = _run(t, g, x, ww, dm, 0.02)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+    # 8 channels: the edge-slot forward, whose slot sums are added in a fixed order
+    w5 = W.WORKLOADS[5]
+    t5 = e3.Table.create(w5.blocks, w5.mul, 3, 3)
+    g5 = W.make_graph(w5, n_atoms=1500)
+    x5, ww5 = W.make_conv(w5, g5, t5.n_paths)
+    dm5 = W.make_grad(w5, g5.n_nodes, t5.D)
+    first = [o.clone() for o in _run(t5, g5, x5, ww5, dm5, 0.03)]
+    for _ in range(9):
+        for a, b in zip(first, _run(t5, g5, x5, ww5, dm5, 0.03)):
+            assert torch.equal(a, b)
     # rows: TP forward / backward
     w2 = W.WORKLOADS[2]
     t2 = e3.Table.create(w2.blocks, w2.mul, 3, 3)

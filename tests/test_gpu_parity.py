@@ -212,6 +212,24 @@ def test_conv_high_l_low_channel_full_size_sampled():
     _conv_check(w, W.make_graph(w), k_nodes=256, k_edges=1024)
 
 
+@pytest.mark.parametrize("blocks,mul,dt", [
+    ("0e+1o+2e+3o", 4, torch.float32),
+    ("0e+1o+2e+3o", 16, torch.float32),
+    ("0e+1o+2e+3o", 32, torch.float32),
+    ("0e+1o+2e+3o", 8, torch.bfloat16),
+    ("0e+1o+2e", 32, torch.float32),
+    ("0e+1o", 4, torch.bfloat16),
+])
+def test_conv_narrow_channel_counts(blocks, mul, dt):
+    """4-32 channels run the edge-slot forward (up to 8 edges of a receiver at once, their
+    partial sums added across slots); a box of 400 atoms with ~30 neighbours puts receivers of
+    1-8 and more slot rounds side by side, and the backward its plain kernel."""
+    irreps = "+".join(f"{mul}x{b}" for b in blocks.split("+"))
+    w = W.Workload(94, "narrow channels", "conv", irreps, 3, 3, n_atoms=400, degree=30.0)
+    g = W.make_graph(w)
+    _conv_check(w, g, tol=TOL_BF16 if dt == torch.bfloat16 else TOL_F32, dtype=dt)
+
+
 def test_conv_irregular_graph_with_empty_receivers():
     w = W.Workload(94, "irregular", "conv", "16x0e+16x1o", 3, 3, n_atoms=0)
     g = random_graph(61, 500, (94, 0), empty_nodes=9)
