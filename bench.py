@@ -229,11 +229,12 @@ def _median(xs):
 
 
 def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: str = "cell",
-                       pad_frac: float = 0.0):
+                       pad_frac: float = 0.0, n_atoms=None):
     """Per-kernel device times of SH, conv forward and conv backward on one conv workload.
     pad_frac > 0: the same graph plus one padding node holding that fraction of all edge slots
     (mostly pad -> pad, 2% pad -> real receivers, 1% real senders -> pad), with NaN inputs on
-    every padding row, run with pad_node set; rates count the real edges."""
+    every padding row, run with pad_node set; rates count the real edges. n_atoms: a smaller box
+    of the same density and degree (profiling)."""
     import torch
 
     import message_passing_gb300 as e3
@@ -242,7 +243,7 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
     from synth import workloads as W
     s = 2 if dt == torch.bfloat16 else 4
     t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
-    g = W.make_graph(wl, order=order)
+    g = W.make_graph(wl, n_atoms=n_atoms, order=order)
     E_real, pad = g.n_edges, -1
     x_np, _ = W.make_conv(wl, g, t.n_paths, edge_ids=np.zeros(0, np.int64))
     if pad_frac > 0:
@@ -673,7 +674,8 @@ def run_ours(args):
                 ("conv4", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak)),
                 ("conv3", lambda: time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak)),
                 ("conv4bf16", lambda: time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak)),
-                ("conv5", lambda: time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak)),
+                ("conv5", lambda: time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak,
+                                                     n_atoms=args.workload_atoms)),
                 ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
                                                    pad_frac=0.25)),
                 ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak))]
@@ -732,6 +734,8 @@ def main():
     ap.add_argument("--workloads", default="all",
                     help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,dbwd (or all)")
     ap.add_argument("--dbwd-atoms", type=int, default=None, help="smaller double-backward case (profiling)")
+    ap.add_argument("--workload-atoms", type=int, default=None,
+                    help="smaller box for the 8-channel workload's timing (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
