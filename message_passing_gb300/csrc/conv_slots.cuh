@@ -11,8 +11,9 @@
 // the slots with a transposing butterfly (fixed order: deterministic) and each lane stores the
 // rows it ends up holding. Each lane computes the couplings of its edge from compile-time CG
 // values next to their use, so the G lanes of an edge repeat that work (G = 2 at 8 channels)
-// instead of every channel lane (the plain kernels' 8). x rows are re-read per path (they stay
-// in L1); the weights of a slot's next edge are prefetched into L2.
+// instead of every channel lane (the plain kernels' 8). Each lane copies its 4 channels of the
+// next edge's sender x rows into its own double-buffered shared-memory slice with cp.async (no
+// warp barrier: a lane reads only what it copied) and prefetches that edge's weights into L2.
 #pragma once
 
 #include "conv_pipe.cuh"
@@ -46,6 +47,10 @@ struct SlotsFit {   // register budget: the output rows of one receiver in regis
 // receivers handled by one 256-thread block
 template <int NQ>
 constexpr int slots_nodes_per_block() { return 8 * Slots<NQ>::NPW; }
+// staged x rows: [buffer][row][lane][4 channels] per warp, each lane reading only its own slice
+constexpr int kSlotRow = 32 * 4;   // elements between rows of one buffer
+template <class Cfg, class T>
+constexpr int slots_fwd_smem() { return 8 * 2 * Cfg::D1 * kSlotRow * int(sizeof(T)); }
 
 
 // Add R per-lane row quads (R a power of two >= SPR) over the SPR edge slots of a node: every
@@ -122,7 +127,7 @@ __device__ __forceinline__ void load_y(const T* __restrict__ ye, float (&yv)[Cfg
 // ------------------------------------------------------------------------------------------
 // acc[zoff + m3] += w * sum_m1 A[m3][m1] x[m1] for every path of one edge (4 channels)
 template <class Cfg, class T, int NQ, int R>
-__device__ __forceinline__ void slots_edge_fwd(const T* __restrict__ xa, const float (&yv)[Cfg::D2],
+__device__ __forceinline__ void slots_edge_fwd(const T* __restrict__ xs, const float (&yv)[Cfg::D2],
                                                const T* __restrict__ we, Q2 (&acc)[R]) {
     sfor<Cfg::NP>([&](auto pp) {
         constexpr int p = decltype(pp)::value;
@@ -134,7 +139,7 @@ __device__ __forceinline__ void slots_edge_fwd(const T* __restrict__ xa, const f
         const Q2 wv = ldg_q2<T>(we + p * NQ);
         Q2 xr[n1];
 #pragma unroll
-        for (int m = 0; m < n1; ++m) xr[m] = ldg_q2<T>(xa + (pi.xoff + m) * NQ);
+        for (int m = 0; m < n1; ++m) xr[m] = lds_q2<T>(xs + (pi.xoff + m) * kSlotRow);
         if constexpr (n1 <= n3) {
 #pragma unroll
             for (int m = 0; m < n1; ++m) xr[m] = q2_mul(xr[m], wv);
@@ -175,6 +180,8 @@ __global__ void __launch_bounds__(256) conv_forward_slots_kernel(int64_t N, int6
     const int c0 = gl * 4;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    extern __shared__ __align__(128) unsigned char slots_smem[];
+    T* xs = reinterpret_cast<T*>(slots_smem) + (threadIdx.x >> 5) * (2 * Cfg::D1 * kSlotRow) + lane * 4;
     for (int64_t b0 = warp * SL::NPW; b0 < N; b0 += nwarp * SL::NPW) {   // warp-uniform
         const int64_t b = b0 + nl;
         int64_t e0 = 0, e1 = 0;
@@ -206,22 +213,41 @@ __global__ void __launch_bounds__(256) conv_forward_slots_kernel(int64_t N, int6
             }
             return -1;
         };
-        for (int64_t it = 0;; ++it) {
-            const int64_t e = next_edge(it);
-            if (!__any_sync(0xffffffffu, e >= 0)) break;   // the warp runs to its largest node
-            if (pad < 0 && gl == 0 && e >= 0 && e + SL::SPR < e1)   // the slot's next edge: weights into L2
-                prefetch_l2<Cfg::NP * NQ * int(sizeof(T))>(w + (e + SL::SPR) * Cfg::NP * NQ);
+        // the sender's x rows of edge e (this lane's 4 channels) into buffer j, one edge ahead;
+        // the weights of that edge into L2
+        auto stage = [&](int64_t e, int j) {
             if (e >= 0) {
                 const int64_t a = __ldg(sender + e);
+                if (a >= 0 && a < N) {
+                    const T* src = x + a * Cfg::D1 * NQ + c0;
+#pragma unroll
+                    for (int r = 0; r < Cfg::D1; ++r) cp_async_slice<T>(xs + (j * Cfg::D1 + r) * kSlotRow, src + r * NQ);
+                }
+                if (gl == 0) prefetch_l2<Cfg::NP * NQ * int(sizeof(T))>(w + e * Cfg::NP * NQ);
+            }
+            cp_async_commit();
+        };
+        int64_t cur = next_edge(0);
+        stage(cur, 0);
+        for (int64_t it = 0;; ++it) {
+            if (!__any_sync(0xffffffffu, cur >= 0)) break;   // the warp runs to its largest node
+            const int64_t nxt = next_edge(it + 1);
+            stage(nxt, int((it + 1) & 1));
+            cp_async_wait<1>();   // this lane's copies for cur are complete
+            if (cur >= 0) {
+                const int64_t a = __ldg(sender + cur);
                 if (a < 0 || a >= N) {
                     if (gl == 0) atomicOr(err, kErrSender);
                 } else {
                     float yv[Cfg::D2];
-                    load_y<Cfg, T>(y + e * Cfg::D2, yv);
-                    slots_edge_fwd<Cfg, T, NQ, R>(x + a * Cfg::D1 * NQ + c0, yv, w + e * Cfg::NP * NQ + c0, acc);
+                    load_y<Cfg, T>(y + cur * Cfg::D2, yv);
+                    slots_edge_fwd<Cfg, T, NQ, R>(xs + int(it & 1) * Cfg::D1 * kSlotRow, yv,
+                                                  w + cur * Cfg::NP * NQ + c0, acc);
                 }
             }
+            cur = nxt;
         }
+        cp_async_wait<0>();
         const int row0 = slot_sum_transposed<R, SL::SPR, SL::G>(acc, es);
         if (b < N) {
             const float2 sc = make_float2(scale, scale);

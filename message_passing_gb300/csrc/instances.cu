@@ -156,9 +156,13 @@ static cudaError_t launch_fwd_slots(int64_t N, int64_t E, const int32_t* rowptr,
                                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
                                     cudaStream_t s) {
     auto k = conv_forward_slots_kernel<Cfg, T, NQ>;
+    constexpr int smem = slots_fwd_smem<Cfg, T>();
+    cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (st != cudaSuccess) return st;
     const int grid = grid_for((const void*)k, kBlock, slots_nodes_per_block<NQ>(), N);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, 0, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m, pad, err);
+    k<<<grid, kBlock, smem, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m, pad,
+                                 err);
     return cudaGetLastError();
 }
 
