@@ -6,7 +6,7 @@ Follows "e3j ...", App. A.3 Eq. (6) (output degrees L = |l - l'| .. l + l' per p
 degrees), App. B.1 (parity selection rule p1 p2 = p3) and App. E.1 (trailing channels:
 row = [feature coordinate][channel]).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * a path is an (x block, l2, l3) triangle with l3 <= out_lmax; its output parity is
   p3 = p1 (-1)^l2 (SH of degree l2 have parity (-1)^l2), so every triangle is kept;
 * paths are ordered by (x block index, l2, l3); that order is the weight index p;
