@@ -47,10 +47,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each traffic entry's kernel is compiled and launched from
+KERNEL_SOURCES = {
+    "conv_fwd": ("conv_pipe.cuh", "kernels.cuh", "cg_table.hpp", "configs.def", "instances.cu"),
+    "conv_bwd": ("conv_pipe.cuh", "kernels.cuh", "cg_table.hpp", "configs.def", "instances.cu"),
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the kernel's sources (all of csrc/ when the kernel has no entry above)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "message_passing_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(d))
+    for n in names:
         with open(os.path.join(d, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -65,7 +74,7 @@ def ncu_traffic(kernel: str, units: float):
     except Exception:
         return None
     ent = tr.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return float(ent["bytes_per_unit"]) * units
 

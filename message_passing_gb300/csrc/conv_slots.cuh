@@ -6,14 +6,15 @@
 // shared by as many channels as possible. Here a lane owns 4 channels (G = Nq / 4 lanes per
 // edge) and a warp works on SPR edges of the same receiver at once ("edge slots", up to 8),
 // plus further receivers when Nq is small (Nq = 4, 8: 4 and 2 receivers per warp). Slot s of
-// receiver b takes its edges s, s + SPR, ... (receiver-stationary, Alg. 2), accumulating all
-// output rows of its 4 channels in registers; at the end the SPR partial sums are added across
-// the slots with a transposing butterfly (fixed order: deterministic) and each lane stores the
-// rows it ends up holding. Each lane computes the couplings of its edge from compile-time CG
-// values next to their use, so the G lanes of an edge repeat that work (G = 2 at 8 channels)
-// instead of every channel lane (the plain kernels' 8). Each lane copies its 4 channels of the
-// next edge's sender x rows into its own double-buffered shared-memory slice with cp.async (no
-// warp barrier: a lane reads only what it copied) and prefetches that edge's weights into L2.
+// receiver b takes its (non-padding) edges s, s + SPR, ... (receiver-stationary, Alg. 2),
+// accumulating all output rows of its 4 channels in registers; at the end the SPR partial sums
+// are added across the slots with a transposing butterfly (fixed order: deterministic) and
+// each lane stores the rows it ends up holding. Each lane computes the couplings of its edge
+// from compile-time CG values next to their use, so the G lanes of an edge repeat that work
+// (G = 2 at 8 channels) instead of every channel lane (the plain kernels' 8). Each lane copies
+// its 4 channels of the next edge's sender x rows into its own double-buffered shared-memory
+// slice with cp.async (no warp barrier: a lane reads only what it copied) and prefetches that
+// edge's weights into L2.
 #pragma once
 
 #include "conv_pipe.cuh"
@@ -41,7 +42,7 @@ constexpr int ilog2(int v) {
 }
 
 template <class Cfg>
-struct SlotsFit {   // register budget: the output rows of one receiver in registers
+struct SlotsFit {   // the output rows of one receiver in registers; staged x rows <= 128 KB
     static constexpr bool value = Cfg::D <= 32 && Cfg::D1 <= 16;
 };
 // receivers handled by one 256-thread block
@@ -125,7 +126,8 @@ __device__ __forceinline__ void load_y(const T* __restrict__ ye, float (&yv)[Cfg
 // ------------------------------------------------------------------------------------------
 // forward
 // ------------------------------------------------------------------------------------------
-// acc[zoff + m3] += w * sum_m1 A[m3][m1] x[m1] for every path of one edge (4 channels)
+// acc[zoff + m3] += w * sum_m1 A[m3][m1] x[m1] for every path of one edge (4 channels); xs is
+// this lane's staged copy of the sender's x rows (row r at xs + r * kSlotRow)
 template <class Cfg, class T, int NQ, int R>
 __device__ __forceinline__ void slots_edge_fwd(const T* __restrict__ xs, const float (&yv)[Cfg::D2],
                                                const T* __restrict__ we, Q2 (&acc)[R]) {
