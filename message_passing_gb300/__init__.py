@@ -130,6 +130,19 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _shape(name, t, *shape):
+    """The kernels index every buffer from the table's sizes and the row/node/edge counts, so a
+    buffer of another shape would be read or written out of bounds: refuse it here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _index_len(name, t, n):
+    """An index array of at least n entries (the graph index arrays hold max(E, 1))."""
+    if t is not None and (t.dim() != 1 or t.shape[0] < n):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected ({n},) or longer")
+
+
 def version() -> str:
     return load().e3gb_version().decode()
 
@@ -212,6 +225,25 @@ class Table:
             self.handle = None
 
 
+def _rows_operands(t: "Table", R: int, x, y, w, names=("x", "y", "w")):
+    _shape(names[0], x, R, t.d1, t.mul)
+    _shape(names[1], y, R, t.d2)
+    _shape(names[2], w, R, t.n_paths, t.mul)
+
+
+def _conv_operands(t: "Table", N: int, E: int, x, y, w, names=("x", "y", "w")):
+    _shape(names[0], x, N, t.d1, t.mul)
+    _shape(names[1], y, E, t.d2)
+    _shape(names[2], w, E, t.n_paths, t.mul)
+
+
+def _csc_shapes(csc, N: int, E: int):
+    cp, ce, cr = csc
+    _shape("csc_ptr", cp, N + 1)
+    _index_len("csc_edge", ce, E)
+    _index_len("csc_recv", cr, E)
+
+
 def sh_forward(vec, lmax: int, out=None, dtype=None, stream=None):
     """y[n, (lmax+1)^2] = real SH of vec[n, 3] (fp32 device tensor)."""
     import torch
@@ -219,7 +251,9 @@ def sh_forward(vec, lmax: int, out=None, dtype=None, stream=None):
     if vec.dtype != torch.float32:
         raise TypeError("vec must be float32")
     dt = dtype or torch.float32
+    _shape("vec", vec, vec.shape[0], 3)
     y = out if out is not None else torch.empty((vec.shape[0], (lmax + 1) ** 2), dtype=dt, device=vec.device)
+    _shape("y", y, vec.shape[0], (lmax + 1) ** 2)
     _check(load().e3gb_sh_forward(lmax, vec.shape[0], _ptr(vec), _ptr(y), _dtype(y), _stream(stream)))
     return y
 
@@ -230,16 +264,25 @@ def sh_backward(vec, dy, lmax: int, out=None, stream=None):
     _contig(vec, dy)
     if vec.dtype != torch.float32:
         raise TypeError("vec must be float32")
-    dvec = out if out is not None else torch.empty((vec.shape[0], 3), dtype=torch.float32, device=vec.device)
+    n = vec.shape[0]
+    _shape("vec", vec, n, 3)
+    _shape("dy", dy, n, (lmax + 1) ** 2)
+    dvec = out if out is not None else torch.empty((n, 3), dtype=torch.float32, device=vec.device)
+    _shape("dvec", dvec, n, 3)
     _f32_out(dvec)
     _check(load().e3gb_sh_backward(lmax, vec.shape[0], _ptr(vec), _ptr(dy), _ptr(dvec), _dtype(dy), _stream(stream)))
     return dvec
 
 
 def tp_forward(t: Table, x, y, w, out=None, stream=None):
+    """z[R, D, mul] (fp32) = sum over paths of w * CG(x, y) per row: x [R, d1, mul],
+    y [R, d2], w [R, n_paths, mul]."""
     import torch
     _contig(x, y, w, out)
-    z = out if out is not None else torch.empty((x.shape[0], t.D, t.mul), dtype=torch.float32, device=x.device)
+    R = x.shape[0]
+    _rows_operands(t, R, x, y, w)
+    z = out if out is not None else torch.empty((R, t.D, t.mul), dtype=torch.float32, device=x.device)
+    _shape("z", z, R, t.D, t.mul)
     _f32_out(z)
     _check(load().e3gb_tp_forward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(z),
                                   _dtype(x, y, w), _stream(stream)))
@@ -247,12 +290,18 @@ def tp_forward(t: Table, x, y, w, out=None, stream=None):
 
 
 def tp_backward(t: Table, x, y, w, dz, out=None, stream=None):
+    """(dx, dy, dw) of tp_forward for the cotangent dz [R, D, mul], all fp32, shaped like
+    x, y, w."""
     import torch
     _contig(x, y, w, dz)
+    R = x.shape[0]
+    _rows_operands(t, R, x, y, w)
+    _shape("dz", dz, R, t.D, t.mul)
     if out is None:
         f = dict(dtype=torch.float32)
         out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f))
     dx, dy, dw = out
+    _rows_operands(t, R, dx, dy, dw, ("dx", "dy", "dw"))
     _f32_out(dx, dy, dw)
     _check(load().e3gb_tp_backward(t.handle, x.shape[0], _ptr(x), _ptr(y), _ptr(w), _ptr(dz), _ptr(dx),
                                    _ptr(dy), _ptr(dw), _dtype(x, y, w, dz), _stream(stream)))
@@ -269,10 +318,12 @@ def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream
     _contig(rowptr, sender)
     E = sender.shape[0]
     dev = rowptr.device
+    _shape("rowptr", rowptr, n_nodes + 1)
     if out is None:
         out = (torch.empty(n_nodes + 1, dtype=torch.int32, device=dev),
                torch.empty(max(E, 1), dtype=torch.int32, device=dev),
                torch.empty(max(E, 1), dtype=torch.int32, device=dev))
+    _csc_shapes(out, n_nodes, E)
     nb = graph_prepare_workspace_bytes(n_nodes)
     ws = workspace if workspace is not None else torch.empty(nb, dtype=torch.uint8, device=dev)
     cp, ce, cr = out
@@ -294,10 +345,12 @@ def graph_prepare_static(rowptr, sender, n_nodes: int, out=None, stream=None):
     _contig(rowptr, sender)
     E = sender.shape[0]
     dev = rowptr.device
+    _shape("rowptr", rowptr, n_nodes + 1)
     if out is None:
         out = (torch.empty(n_nodes + 1, dtype=torch.int32, device=dev),
                torch.empty(max(E, 1), dtype=torch.int32, device=dev),
                torch.empty(max(E, 1), dtype=torch.int32, device=dev))
+    _csc_shapes(out, n_nodes, E)
     cp, ce, cr = out
     _check(load().e3gb_graph_prepare_static(n_nodes, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(cp),
                                             _ptr(ce) if E else None, _ptr(cr) if E else None, _stream(stream)))
@@ -310,7 +363,10 @@ def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stre
     import torch
     _contig(rowptr, sender, x, y, w)
     N, E = x.shape[0], sender.shape[0]
+    _shape("rowptr", rowptr, N + 1)
+    _conv_operands(t, N, E, x, y, w)
     m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=torch.float32, device=x.device)
+    _shape("m", m, N, t.D, t.mul)
     _f32_out(m)
     _check(load().e3gb_conv_forward(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
                                     _ptr(y) if E else None, _ptr(w) if E else None, float(scale), int(pad_node), _ptr(m),
@@ -325,10 +381,14 @@ def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=Non
     cp, ce, cr = csc
     _contig(x, y, w, dm)
     N, E = x.shape[0], y.shape[0]
+    _csc_shapes(csc, N, E)
+    _conv_operands(t, N, E, x, y, w)
+    _shape("dm", dm, N, t.D, t.mul)
     if out is None:
         f = dict(dtype=torch.float32)
         out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f))
     dx, dy, dw = out
+    _conv_operands(t, N, E, dx, dy, dw, ("dx", "dy", "dw"))
     _f32_out(dx, dy, dw)
     _check(load().e3gb_conv_backward(t.handle, N, E, _ptr(cp), _ptr(ce) if E else None, _ptr(cr) if E else None,
                                      _ptr(x), _ptr(y) if E else None, _ptr(w) if E else None, _ptr(dm),
@@ -346,11 +406,19 @@ def conv_double_backward(t: Table, rowptr, sender, csc, x, y, w, dm, delta_dx, d
     cp, ce, cr = csc
     _contig(rowptr, sender, x, y, w, dm, delta_dx, delta_dy, delta_dw)
     N, E = x.shape[0], y.shape[0]
+    _shape("rowptr", rowptr, N + 1)
+    _shape("sender", sender, E)
+    _csc_shapes(csc, N, E)
+    _conv_operands(t, N, E, x, y, w)
+    _conv_operands(t, N, E, delta_dx, delta_dy, delta_dw, ("delta_dx", "delta_dy", "delta_dw"))
+    _shape("dm", dm, N, t.D, t.mul)
     if out is None:
         f = dict(dtype=torch.float32)
         out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(w, **f),
                torch.empty_like(dm, **f))
     gx, gy, gw, gdm = out
+    _conv_operands(t, N, E, gx, gy, gw, ("delta_x", "delta_y", "delta_w"))
+    _shape("delta_dm", gdm, N, t.D, t.mul)
     _f32_out(gx, gy, gw, gdm)
     e = (lambda a: _ptr(a) if E else None)
     _check(load().e3gb_conv_double_backward(
