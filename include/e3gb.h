@@ -24,7 +24,9 @@
  * legacy default stream) and the call returns without synchronising. Channel-vector arrays
  * (x, w, dz, dm, and every fp32 output) must be 16-byte aligned, or 8-byte aligned when they
  * are bf16 inputs; y and dy need element alignment; buffers must not alias each other.
- * Outputs are always fp32 and are overwritten, never accumulated into.
+ * Every buffer must hold the elements its layout above implies for the given counts: the
+ * library receives bare pointers and cannot check sizes (the Python binding checks tensor
+ * shapes before each call). Outputs are always fp32 and are overwritten, never accumulated into.
  *
  * Errors: each call checks its arguments on the host and returns a status; the message of
  * the last failure on the calling thread is e3gb_last_error(). Index errors found on the
