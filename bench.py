@@ -10,7 +10,11 @@ run (forward and backward, own timed loops) and reported under "tp" (the "TP fwd
 HBM GB/s" half). Inputs are resident in HBM; the edge weights alone (31.5 GB) exceed L2
 (129 MB), so no flush is needed between steps. "e2e" measures the same step through the
 public API with host buffers: pinned host -> device copies of the step's inputs and
-device -> host copies of all outputs inside the timed region.
+device -> host copies of all outputs inside the timed region (consecutive steps overlap their
+copies and compute on three streams with two device buffer sets).
+
+Profiling options shrink single parts of the run (--atoms for the main step, --tp-rows,
+--workload-atoms for the 8-channel workload, --dbwd-atoms, --workloads to pick timings).
 
 Throughput accounting follows "e3j ...", Sec. 3 Eq. (9): (bytes of inputs + outputs) /
 runtime, backward counting input primals, output cotangents and input cotangents.
