@@ -14,6 +14,9 @@ under rotations whose Wigner matrices are fitted from harmonic values; equivaria
 tensor product and convolution, a scalar-only case that is a plain weighted SpMM, the
 Euler identity <dz, z> = <dx, x> = <dy, y> = <dw, w> and central finite differences for the
 backward passes, and the convolution as a scatter-sum (numpy.add.at) of per-edge products.
+The radial edge scalars (radial.py: Bessel basis, polynomial envelope, one SiLU hidden layer)
+are pinned by scipy's spherical Bessel functions, quadrature, the envelope's defining
+conditions, finite differences and the forces of the radial-weighted convolution.
 """
 from __future__ import annotations
 
@@ -26,6 +29,7 @@ import numpy as np
 
 from .cg import cg_block
 from .coo import cg_records, coo_tp_backward, coo_tp_forward
+from . import radial
 from .paths import Table, make_table
 from .sh import sh, sh_grad
 
@@ -267,7 +271,7 @@ def conv_double_backward(t: Table, rowptr, sender, x, y, w, dm, ddx, ddy, ddw, s
     return dx2 + dx3, dy1 + dy3, dw1 + dw2, ddm
 
 
-__all__ = ["sh", "sh_grad", "cg_block", "cg_records", "coo_tp_forward", "coo_tp_backward", "table", "tp_forward",
+__all__ = ["radial", "sh", "sh_grad", "cg_block", "cg_records", "coo_tp_forward", "coo_tp_backward", "table", "tp_forward",
            "tp_backward", "conv_forward",
            "conv_backward_edges", "conv_backward_dx", "conv_double_backward", "build", "num_threads",
            "receivers_of"]

@@ -7,7 +7,8 @@ features, edge weights, upstream gradients, a receiver-sorted CSR graph).
 
 Seeding: every array comes from ``numpy.random.Generator(PCG64(SeedSequence(key)))`` with
 ``key = [workload_id, stream_id(, chunk)]``. Streams: 0 positions / unit vectors, 1 node or
-row features x, 2 weights w, 3 upstream gradients (dz or dm). Weights and gradients are
+row features x, 2 weights w, 3 upstream gradients (dz or dm), 4 the parameters of the radial
+network that produces the weights from edge lengths. Weights and gradients are
 drawn in chunks of ``CHUNK`` rows so that any subset of rows can be regenerated without
 drawing the rest (the full-size parity tests sample rows that way).
 
@@ -27,7 +28,7 @@ import os
 import numpy as np
 
 CHUNK = 4096          # rows (or edges) per independently seeded chunk
-STREAM_POS, STREAM_X, STREAM_W, STREAM_GRAD = 0, 1, 2, 3
+STREAM_POS, STREAM_X, STREAM_W, STREAM_GRAD, STREAM_RADIAL = 0, 1, 2, 3, 4
 
 
 def rng(*key: int) -> np.random.Generator:

@@ -11,8 +11,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import (STREAM_GRAD, STREAM_POS, STREAM_W, STREAM_X, Graph, box_graph, normal_rows,
-               unit_vectors)
+from . import (STREAM_GRAD, STREAM_POS, STREAM_RADIAL, STREAM_W, STREAM_X, Graph, box_graph, normal_rows,
+               rng, unit_vectors)
 
 
 def parse_irreps(s: str) -> tuple[int, list[tuple[int, int]]]:
@@ -116,3 +116,13 @@ def make_conv(w: Workload, g: Graph, n_paths: int, edge_ids: np.ndarray | None =
     x = normal_rows(g.n_nodes, (w.d1, w.mul), (w.wid, STREAM_X))
     ww = normal_rows(g.n_edges, (P, w.mul), (w.wid, STREAM_W), weight_scale(w, P), rows=edge_ids)
     return x, ww
+
+
+def make_radial(w: Workload, n_paths: int, n_basis: int = 8, hidden: int = 8):
+    """Parameters of the radial network (float32): W1[n_basis, hidden] ~ N(0, 2^2) and
+    W2[hidden, P, mul] ~ N(0, 1/(hidden P)), so that the weights it produces have roughly the
+    spread of the drawn ones."""
+    r = rng(w.wid, STREAM_RADIAL)
+    W1 = (2.0 * r.standard_normal((n_basis, hidden))).astype(np.float32)
+    W2 = (r.standard_normal((hidden, n_paths, w.mul)) / math.sqrt(hidden * n_paths)).astype(np.float32)
+    return W1, W2
