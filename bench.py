@@ -280,6 +280,16 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
     m = torch.empty((N, D, Nq), device=dev, **f32)
     dx, dy, dw = torch.empty_like(xd, **f32), torch.empty_like(y, **f32), torch.empty_like(wd, **f32)
     csc = e3.graph_prepare(rp, sd, N)
+    # the sender-major index (once per graph, so outside the step): its own timed loop
+    gws = torch.empty(e3.graph_prepare_workspace_bytes(N, E), dtype=torch.uint8, device=dev)
+    evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        evg[k][0].record(stream)
+        e3.graph_prepare(rp, sd, N, out=csc, workspace=gws, stream=stream)
+        evg[k][1].record(stream)
+    torch.cuda.synchronize()
+    tgp = _median([e[0].elapsed_time(e[1]) for e in evg[2:]]) / 1e3
+    del gws
     dvec = torch.empty_like(vec)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps + 2)]
     for k in range(reps + 2):
@@ -308,7 +318,7 @@ def time_conv_workload(wl, dt, dev, stream, reps: int, hbm_peak: float, order: s
     E = E_real
     name = wl.name if pad < 0 else f"{wl.name} + {pad_frac:.0%} padding edge slots on one padding node"
     out = {"workload": name, "dtype": "bf16" if s == 2 else "f32", "atoms": N, "edges": E,
-           "sh_ms": tsh * 1e3,
+           "sh_ms": tsh * 1e3, "graph_prepare_ms": tgp * 1e3,
            "sh_backward": {"ms": tshb * 1e3, "alg_GBps": bshb / tshb / 1e9, "frac": bshb / tshb / 1e9 / hbm_peak},
            "fwd": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bf / tf / 1e9, "frac": bf / tf / 1e9 / hbm_peak},
            "bwd": {"ms": tb * 1e3, "edges_per_s": E / tb, "alg_GBps": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak},
@@ -374,6 +384,87 @@ def time_double_backward(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=No
            "composition_six_calls": {"ms": tc * 1e3, "edges_per_s": E / tc},
            "speedup_vs_composition": tc / tf}
     del xd, ddx, y, ddy, wd, ddw, dmd, out, tmp_m, tmp_b
+    torch.cuda.empty_cache()
+    return res
+
+
+# FP32 FMA peak of a GB300 derived from its unit counts and the maximum SM clock: 152 SMs x
+# 128 FP32 lanes x 2 flop x 2.07 GHz (the roofline of the arithmetic-bound radial kernels)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def radial_flops(E, nnz, P, D, Nq, H):
+    """Algorithmic flops per pass: the convolution's 2 Nq (nnz + D) per edge (the coupling
+    entries applied to the channels, and the weighted sums) plus the output layer of the radial
+    network formed in the kernel, 2 H P Nq per edge; the backward does the weights once, their
+    cotangent once and about twice the forward's convolution work."""
+    conv = 2.0 * Nq * (nnz + D) * E
+    wts = 2.0 * H * P * Nq * E
+    return conv + wts, 2.0 * conv + 2.0 * wts
+
+
+def time_radial_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None):
+    """The radial form of the convolution step (e3j App. E.1, the edge scalars produced by a
+    radial network; App. A.3 "Linear mixing" fused into message passing): SH + the radial
+    hidden layer + conv forward and backward with the weights formed in the kernels (w and dw
+    never reach memory) + forces (SH backward plus the radial backward)."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import STREAM_GRAD, device_normal
+    from synth import workloads as W
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    g = W.make_graph(wl, n_atoms=n_atoms)
+    N, E, Nq, P, D = g.n_nodes, g.n_edges, wl.mul, t.n_paths, t.D
+    H = e3.RADIAL_HIDDEN
+    scale = N / E
+    rc = float(g.cutoff)
+    x_np, _ = W.make_conv(wl, g, P, edge_ids=np.zeros(0, np.int64))
+    W1, W2 = W.make_radial(wl, P, hidden=H)
+    xd = torch.from_numpy(x_np).to(dev)
+    vec = torch.from_numpy(g.vec.astype(np.float32)).to(dev)
+    rp = torch.from_numpy(g.rowptr).to(dev)
+    sd = torch.from_numpy(g.sender).to(dev)
+    W1d, W2d = torch.from_numpy(W1).to(dev), torch.from_numpy(W2).to(dev)
+    dmd = device_normal((N, D, Nq), (wl.wid, STREAM_GRAD), device=dev)
+    csc = e3.graph_prepare(rp, sd, N)
+    y = torch.empty((E, t.d2), device=dev)
+    h = torch.empty((E, H), device=dev)
+    m = torch.empty((N, D, Nq), device=dev)
+    dx, dy, dh = torch.empty_like(xd), torch.empty_like(y), torch.empty_like(h)
+    dvec = torch.empty_like(vec)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps + 2)]
+    for k in range(reps + 2):
+        ev[k][0].record(stream)
+        e3.sh_forward(vec, wl.sh_lmax, out=y, stream=stream)
+        e3.radial_hidden(vec, W1d, rc, out=h, stream=stream)
+        ev[k][1].record(stream)
+        e3.conv_forward_radial(t, rp, sd, xd, y, h, W2d, scale, out=m, stream=stream)
+        ev[k][2].record(stream)
+        e3.conv_backward_radial(t, csc, xd, y, h, W2d, dmd, scale, out=(dx, dy, dh), stream=stream)
+        ev[k][3].record(stream)
+        e3.sh_backward(vec, dy, wl.sh_lmax, out=dvec, stream=stream)
+        e3.radial_backward(vec, W1d, rc, dh, out=dvec, accumulate=True, stream=stream)
+        ev[k][4].record(stream)
+    torch.cuda.synchronize()
+    e3.check_device_status()
+    med = lambda i, j: _median([e[i].elapsed_time(e[j]) for e in ev[2:]]) / 1e3
+    tpre, tf, tb, tforce = med(0, 1), med(1, 2), med(2, 3), med(3, 4)
+    ff, fb = radial_flops(E, t.nnz, P, D, Nq, H)
+    # bytes the fused kernels move (no w, no dw): x and m (dx, dm) once per node, y, h, the
+    # indices and dy, dh once per edge, W2 once
+    bf = 4 * (N * (t.d1 + D) * Nq + E * (t.d2 + H + 1) + N + 1 + H * P * Nq)
+    bb = 4 * (N * (2 * t.d1 + D) * Nq + E * (2 * t.d2 + 2 * H + 2) + N + 1 + H * P * Nq)
+    res = {"workload": wl.name + " (radial edge scalars: Bessel basis x8, SiLU hidden layer of 8, weights formed in the kernels)",
+           "dtype": "f32", "atoms": N, "edges": E, "hidden": H, "sh_and_hidden_ms": tpre * 1e3,
+           "fwd": {"ms": tf * 1e3, "edges_per_s": E / tf, "alg_GBps": bf / tf / 1e9,
+                   "TFLOPs": ff / tf / 1e12, "frac_fp32_peak": ff / tf / 1e12 / FP32_PEAK_TFLOPS},
+           "bwd": {"ms": tb * 1e3, "edges_per_s": E / tb, "alg_GBps": bb / tb / 1e9,
+                   "TFLOPs": fb / tb / 1e12, "frac_fp32_peak": fb / tb / 1e12 / FP32_PEAK_TFLOPS},
+           "forces_ms": tforce * 1e3,
+           "step_edges_per_s": E / (tpre + tf + tb + tforce),
+           "fp32_peak_TFLOPs": FP32_PEAK_TFLOPS}
+    del xd, vec, dmd, y, h, m, dx, dy, dh, dvec, W1d, W2d
     torch.cuda.empty_cache()
     return res
 
@@ -621,7 +712,7 @@ def run_ours(args):
                 ts = {k: torch.empty_like(v) for k, v in
                       dict(vec=vec, rp=rp, sd=sd, x=xd, w=wd, dm=dmd, y=y, m=m, dx=dx, dy=dy, dw=dw).items()}
                 ts["csc"] = tuple(torch.empty_like(c) for c in csc)
-            ts["ws"] = torch.empty(e3.graph_prepare_workspace_bytes(N), dtype=torch.uint8, device=dev)
+            ts["ws"] = torch.empty(e3.graph_prepare_workspace_bytes(N, E), dtype=torch.uint8, device=dev)
             return ts
         sets = [dev_set(True), dev_set(False)]
         # (non-blocking streams: work on the legacy default stream would serialise with the copies)
@@ -691,7 +782,9 @@ def run_ours(args):
                                                      n_atoms=args.workload_atoms)),
                 ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
                                                    pad_frac=0.25)),
-                ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak))]
+                ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak)),
+                ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak,
+                                                         n_atoms=args.atoms))]
         others = [f() for k, f in jobs if "all" in want or k in want]
         if "all" in want or "dbwd" in want:
             double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak, n_atoms=args.dbwd_atoms)

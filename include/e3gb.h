@@ -135,25 +135,31 @@ e3gb_status e3gb_tp_backward(const e3gb_table *t, int64_t rows, const void *x, c
                              const void *w, const void *dz, void *dx, void *dy, void *dw,
                              e3gb_dtype dtype, void *stream);
 
-/* Workspace (bytes) that e3gb_graph_prepare needs for n_nodes nodes. */
-size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes);
+/* Workspace (bytes) that e3gb_graph_prepare needs for a graph of n_nodes nodes and n_edges
+ * edges (about n_edges bytes: the sort's per-tile digit counts). */
+size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes, int64_t n_edges);
 
 /* Sender-major index of a receiver-sorted CSR graph (rowptr [n_nodes+1], sender [n_edges],
  * receiver b owns edges [rowptr[b], rowptr[b+1])). Writes csc_ptr [n_nodes+1], and for the
  * k-th edge in sender order csc_edge[k] (its CSR edge id) and csc_recv[k] (its receiver);
  * edges of one sender keep increasing edge id (stable). Used by the backward convolution to
  * sum dx per sender without atomics (the transposed graph of Eq. 16). All arrays are
- * device arrays. A sender outside [0, n_nodes) is left out of the index and flagged in the
- * device error word. workspace: device memory of at least
- * e3gb_graph_prepare_workspace_bytes(n_nodes) bytes, 16-byte aligned; its contents on entry
- * do not matter. */
+ * device arrays. The work is linear in n_edges + n_nodes whatever the degrees (a padding
+ * node that sends most edges costs what any other edges cost): a stable radix sort of the
+ * edge ids by sender, ceil(bits(n_nodes)/8) passes. Edges outside [rowptr[0], rowptr[n_nodes])
+ * and edges whose sender is outside [0, n_nodes) are left out of the index (the latter also
+ * flagged in the device error word); the entries past csc_ptr[n_nodes] are -1. A rowptr
+ * segment with a negative start, a decreasing pointer or an end past n_edges is flagged; the
+ * index is then unspecified but every entry stays in range. workspace: device memory of at
+ * least e3gb_graph_prepare_workspace_bytes(n_nodes, n_edges) bytes, 16-byte aligned; its
+ * contents on entry do not matter. */
 e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t *rowptr,
                                const int32_t *sender, int32_t *csc_ptr, int32_t *csc_edge,
                                int32_t *csc_recv, void *workspace, size_t ws_bytes,
                                void *stream);
 
-/* Largest n_nodes that e3gb_graph_prepare_static accepts. */
-#define E3GB_STATIC_PREPARE_MAX_NODES 1048575
+/* Size of the library's own scratch array behind e3gb_graph_prepare_static. */
+#define E3GB_STATIC_PREPARE_SCRATCH_BYTES (4u << 20)
 
 /* e3gb_graph_prepare for callers that cannot allocate device memory. The paper has no
  * counterpart: this entry point exists for programs that must not call cudaMalloc after
@@ -161,12 +167,14 @@ e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t *
  * plugin inside a host that owns every allocation and offers it no allocator, or a
  * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
  * synchronisation. It computes exactly what e3gb_graph_prepare computes, but keeps the
- * per-node counters in a 4 MiB array inside the library (one per device that loads the
- * library, held until the process exits) instead of a caller workspace; it allocates
- * nothing. Limit: n_nodes <= E3GB_STATIC_PREPARE_MAX_NODES, else E3GB_ERR_INVALID_ARG.
- * The first call on a device looks up the array's device address on that device; make that
- * first call before any stream capture. All calls share the one array, and the call clears
- * it on the stream before use: calls that overlap on the GPU (on different streams, or from
+ * sort's digit counts in a 4 MiB array inside the library (E3GB_STATIC_PREPARE_SCRATCH_BYTES,
+ * one per device that loads the library, held until the process exits) instead of a caller
+ * workspace; it allocates nothing. The array holds the counts of at most ~4,000 tiles, so
+ * above ~4 M edges each tile covers more edges (fewer warps share the sort, same result).
+ * Sizes: n_nodes, n_edges < 2^31-1, else E3GB_ERR_INVALID_ARG. The first call on a device
+ * looks up the array's device address on that device; make that first call before any
+ * stream capture. All calls share the one array (every count is written before it is read,
+ * so nothing needs clearing): calls that overlap on the GPU (on different streams, or from
  * different threads) race on it and must be serialised by the caller. */
 e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const int32_t *rowptr,
                                       const int32_t *sender, int32_t *csc_ptr, int32_t *csc_edge,
@@ -227,6 +235,55 @@ e3gb_status e3gb_conv_double_backward(const e3gb_table *t, int64_t n_nodes, int6
                                       int64_t pad_node, void *delta_x, void *delta_y,
                                       void *delta_w, void *delta_dm, e3gb_dtype dtype,
                                       void *stream);
+
+/* Radial edge scalars (e3j, App. E.1 notation for the edge scalars s: "usually" an MLP on a
+ * radial embedding of the interatomic distance, projected to the paths and channels of each
+ * edge; App. A.3 "Linear mixing": that scalar mixing fused into message passing). The pages
+ * fix neither the embedding nor the network; this library reads them as
+ *   b_n(d) = sqrt(2/r_cut) sin(n pi d / r_cut) / d * u(d / r_cut),  n = 1..n_basis
+ *   u(x)   = 1 - 28 x^6 + 48 x^7 - 21 x^8 (x < 1), 0 beyond    (smooth cutoff, p = 6)
+ *   h[e,k] = silu(sum_n b_n(|vec[e]|) W1[n,k]),  w[e,p,q] = sum_k h[e,k] W2[k,p,q]
+ * (no biases; d -> 0 takes the limit sqrt(2/r_cut) n pi / r_cut). The hidden layer is computed
+ * here; the output layer, the large one, is evaluated inside e3gb_conv_*_radial so that w
+ * never reaches device memory.
+ *
+ * e3gb_radial_hidden: h [n_edges, hidden] from vec [n_edges, 3] and W1 [n_basis, hidden]
+ * (float64 arithmetic, fp32 result). n_basis and hidden in [1, 16], r_cut > 0, else
+ * E3GB_ERR_INVALID_ARG. All pointers are device pointers. */
+e3gb_status e3gb_radial_hidden(int64_t n_edges, const float *vec, const float *W1, int32_t n_basis,
+                               int32_t hidden, float r_cut, float *h, void *stream);
+
+/* e3gb_radial_backward: dvec[e] = d <dh[e], h[e]> / d vec[e], the force contribution of the
+ * radial weights, from the cotangent dh [n_edges, hidden] (e3gb_conv_backward_radial's dh).
+ * Radial: (sum_k dh[e,k] silu'(a_k) sum_n b_n'(d) W1[n,k]) vec[e] / |vec[e]|; zero for
+ * |vec[e]| < 1e-12. accumulate != 0 adds to dvec (for example to e3gb_sh_backward's output)
+ * instead of overwriting it. */
+e3gb_status e3gb_radial_backward(int64_t n_edges, const float *vec, const float *W1, int32_t n_basis,
+                                 int32_t hidden, float r_cut, const float *dh, float *dvec,
+                                 int32_t accumulate, void *stream);
+
+/* e3gb_conv_forward with the edge weights produced in the kernel from the hidden activations
+ * h [n_edges, hidden] (16-byte aligned rows) and the output layer W2 [hidden, P, Nq] (device,
+ * 16-byte aligned): w[e,p,q] = sum_k h[e,k] W2[k,p,q], never written out. Otherwise as
+ * e3gb_conv_forward (padding, scale, fixed order, m fully overwritten). Built for fp32
+ * (x, y, m) and hidden = 8: other values give E3GB_ERR_UNSUPPORTED, and so does a W2 larger
+ * than one block's shared memory (hidden * P * Nq * 4 > 227 KiB). */
+e3gb_status e3gb_conv_forward_radial(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                                     const int32_t *rowptr, const int32_t *sender, const void *x,
+                                     const void *y, const float *h, const float *W2, int32_t hidden,
+                                     float scale, int64_t pad_node, void *m, e3gb_dtype dtype,
+                                     void *stream);
+
+/* Its VJP: dx and dy as e3gb_conv_backward, and instead of dw the cotangent of the hidden
+ * activations dh[e,k] = sum_{p,q} W2[k,p,q] dw[e,p,q] [n_edges, hidden] (dw itself never
+ * reaches memory). Padding edges get zero dy and dh rows. Deterministic, no atomics. Same
+ * limits as e3gb_conv_forward_radial. */
+e3gb_status e3gb_conv_backward_radial(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                                      const int32_t *csc_ptr, const int32_t *csc_edge,
+                                      const int32_t *csc_recv, const void *x, const void *y,
+                                      const float *h, const float *W2, int32_t hidden,
+                                      const void *dm, float scale, int64_t pad_node, void *dx,
+                                      void *dy, float *dh, e3gb_dtype dtype, void *stream);
 
 /* Tensor product with arbitrary sparse coefficients on rows (e3j App. E.1 Eq. (10)-(11),
  * Alg. 1: C as a COO list of records), the general bilinear primitive of which the CG

@@ -29,8 +29,12 @@ SYMBOLS = (
     "e3gb_tp_forward", "e3gb_tp_backward", "e3gb_graph_prepare_workspace_bytes",
     "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
     "e3gb_conv_double_backward", "e3gb_coo_tp_forward", "e3gb_coo_tp_backward",
+    "e3gb_radial_hidden", "e3gb_radial_backward", "e3gb_conv_forward_radial", "e3gb_conv_backward_radial",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
 )
+
+# hidden width the radial convolution kernels are built for
+RADIAL_HIDDEN = 8
 
 
 class E3GBError(RuntimeError):
@@ -70,7 +74,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_sh_backward": (i32, [i32, i64, vp, vp, vp, i32, vp]),
         "e3gb_tp_forward": (i32, [vp, i64, vp, vp, vp, vp, i32, vp]),
         "e3gb_tp_backward": (i32, [vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp]),
-        "e3gb_graph_prepare_workspace_bytes": (szt, [i64]),
+        "e3gb_graph_prepare_workspace_bytes": (szt, [i64, i64]),
         "e3gb_graph_prepare": (i32, [i64, i64, vp, vp, vp, vp, vp, vp, szt, vp]),
         "e3gb_graph_prepare_static": (i32, [i64, i64, vp, vp, vp, vp, vp, vp]),
         "e3gb_conv_forward": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, i64, vp, i32, vp]),
@@ -80,6 +84,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_coo_tp_forward": (i32, [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp]),
         "e3gb_coo_tp_backward": (i32, [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                        vp]),
+        "e3gb_radial_hidden": (i32, [i64, vp, vp, i32, i32, f32, vp, vp]),
+        "e3gb_radial_backward": (i32, [i64, vp, vp, i32, i32, f32, vp, vp, i32, vp]),
+        "e3gb_conv_forward_radial": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, i32, f32, i64, vp, i32, vp]),
+        "e3gb_conv_backward_radial": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp, f32, i64, vp, vp, vp,
+                                            i32, vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
         "e3gb_last_error": (ctypes.c_char_p, []),
         "e3gb_version": (ctypes.c_char_p, []),
@@ -308,8 +317,8 @@ def tp_backward(t: Table, x, y, w, dz, out=None, stream=None):
     return dx, dy, dw
 
 
-def graph_prepare_workspace_bytes(n_nodes: int) -> int:
-    return int(load().e3gb_graph_prepare_workspace_bytes(n_nodes))
+def graph_prepare_workspace_bytes(n_nodes: int, n_edges: int) -> int:
+    return int(load().e3gb_graph_prepare_workspace_bytes(n_nodes, n_edges))
 
 
 def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream=None):
@@ -324,7 +333,7 @@ def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream
                torch.empty(max(E, 1), dtype=torch.int32, device=dev),
                torch.empty(max(E, 1), dtype=torch.int32, device=dev))
     _csc_shapes(out, n_nodes, E)
-    nb = graph_prepare_workspace_bytes(n_nodes)
+    nb = graph_prepare_workspace_bytes(n_nodes, E)
     ws = workspace if workspace is not None else torch.empty(nb, dtype=torch.uint8, device=dev)
     cp, ce, cr = out
     _check(load().e3gb_graph_prepare(n_nodes, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(cp),
@@ -333,13 +342,13 @@ def graph_prepare(rowptr, sender, n_nodes: int, out=None, workspace=None, stream
     return cp, ce, cr
 
 
-STATIC_PREPARE_MAX_NODES = 1048575
+STATIC_PREPARE_SCRATCH_BYTES = 4 << 20
 
 
 def graph_prepare_static(rowptr, sender, n_nodes: int, out=None, stream=None):
     """graph_prepare without a workspace, for callers that cannot allocate device memory:
-    the library keeps the counters in its own static device array (at most
-    STATIC_PREPARE_MAX_NODES nodes; calls overlapping on the GPU race on it). Pass ``out``
+    the library keeps the sort's digit counts in its own static device array of
+    STATIC_PREPARE_SCRATCH_BYTES (calls overlapping on the GPU race on it). Pass ``out``
     to avoid allocating the outputs here too."""
     import torch
     _contig(rowptr, sender)
@@ -396,6 +405,96 @@ def conv_backward(t: Table, csc, x, y, w, dm, scale: float, out=None, stream=Non
                                      _ptr(dw) if E else None,
                                      _dtype(x, dm, *((y, w) if E else ())), _stream(stream)))
     return dx, dy, dw
+
+
+def radial_hidden(vec, W1, r_cut: float, out=None, stream=None):
+    """h [E, hidden] = silu(bessel_basis(|vec|) @ W1): the hidden layer of the radial network
+    (W1 [n_basis, hidden], fp32 device tensors)."""
+    import torch
+    _contig(vec, W1)
+    E = vec.shape[0]
+    _shape("vec", vec, E, 3)
+    nb, H = W1.shape
+    h = out if out is not None else torch.empty((E, H), dtype=torch.float32, device=vec.device)
+    _shape("h", h, E, H)
+    for n, a in (("vec", vec), ("W1", W1), ("h", h)):
+        if a.dtype != torch.float32:
+            raise TypeError(f"{n} must be float32")
+    _check(load().e3gb_radial_hidden(E, _ptr(vec) if E else None, _ptr(W1), nb, H, float(r_cut),
+                                     _ptr(h) if E else None, _stream(stream)))
+    return h
+
+
+def radial_backward(vec, W1, r_cut: float, dh, out=None, accumulate: bool = False, stream=None):
+    """dvec [E, 3] = d<dh, h>/dvec (forces through the radial weights); accumulate adds to out."""
+    import torch
+    _contig(vec, W1, dh)
+    E = vec.shape[0]
+    nb, H = W1.shape
+    _shape("vec", vec, E, 3)
+    _shape("dh", dh, E, H)
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs out")
+        out = torch.empty((E, 3), dtype=torch.float32, device=vec.device)
+    _shape("dvec", out, E, 3)
+    _check(load().e3gb_radial_backward(E, _ptr(vec) if E else None, _ptr(W1), nb, H, float(r_cut),
+                                       _ptr(dh) if E else None, _ptr(out) if E else None, int(bool(accumulate)),
+                                       _stream(stream)))
+    return out
+
+
+def _radial_operands(t: "Table", E: int, h, W2):
+    _shape("h", h, E, RADIAL_HIDDEN)
+    _shape("W2", W2, RADIAL_HIDDEN, t.n_paths, t.mul)
+
+
+def conv_forward_radial(t: Table, rowptr, sender, x, y, h, W2, scale: float, out=None, stream=None,
+                        pad_node: int = -1):
+    """conv_forward with w[e] = h[e] @ W2 formed inside the kernel (never stored); fp32."""
+    import torch
+    _contig(rowptr, sender, x, y, h, W2)
+    N, E = x.shape[0], sender.shape[0]
+    _shape("rowptr", rowptr, N + 1)
+    _shape("x", x, N, t.d1, t.mul)
+    _shape("y", y, E, t.d2)
+    _radial_operands(t, E, h, W2)
+    m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=torch.float32, device=x.device)
+    _shape("m", m, N, t.D, t.mul)
+    _f32_out(m, h, W2)
+    _check(load().e3gb_conv_forward_radial(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
+                                           _ptr(y) if E else None, _ptr(h) if E else None, _ptr(W2), RADIAL_HIDDEN,
+                                           float(scale), int(pad_node), _ptr(m), _dtype(x, *((y,) if E else ())),
+                                           _stream(stream)))
+    return m
+
+
+def conv_backward_radial(t: Table, csc, x, y, h, W2, dm, scale: float, out=None, stream=None, pad_node: int = -1):
+    """Returns (dx, dy, dh): conv_backward with dw folded into dh = sum_{p,q} W2 dw (dw never stored)."""
+    import torch
+    cp, ce, cr = csc
+    _contig(x, y, h, W2, dm)
+    N, E = x.shape[0], y.shape[0]
+    _csc_shapes(csc, N, E)
+    _shape("x", x, N, t.d1, t.mul)
+    _shape("y", y, E, t.d2)
+    _radial_operands(t, E, h, W2)
+    _shape("dm", dm, N, t.D, t.mul)
+    if out is None:
+        f = dict(dtype=torch.float32)
+        out = (torch.empty_like(x, **f), torch.empty_like(y, **f), torch.empty_like(h, **f))
+    dx, dy, dh = out
+    _shape("dx", dx, N, t.d1, t.mul)
+    _shape("dy", dy, E, t.d2)
+    _shape("dh", dh, E, RADIAL_HIDDEN)
+    _f32_out(dx, dy, dh, h, W2)
+    _check(load().e3gb_conv_backward_radial(t.handle, N, E, _ptr(cp), _ptr(ce) if E else None,
+                                            _ptr(cr) if E else None, _ptr(x), _ptr(y) if E else None,
+                                            _ptr(h) if E else None, _ptr(W2), RADIAL_HIDDEN, _ptr(dm), float(scale),
+                                            int(pad_node), _ptr(dx), _ptr(dy) if E else None,
+                                            _ptr(dh) if E else None, _dtype(x, dm, *((y,) if E else ())),
+                                            _stream(stream)))
+    return dx, dy, dh
 
 
 def conv_double_backward(t: Table, rowptr, sender, csc, x, y, w, dm, delta_dx, delta_dy, delta_dw, scale: float,

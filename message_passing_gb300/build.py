@@ -56,9 +56,10 @@ def _stale(obj: str, deps: list[str]) -> bool:
 def units() -> list[tuple[str, str, list[str]]]:
     """(source, object, extra flags)"""
     u = [(os.path.join(CSRC, s), os.path.join(OBJDIR, s.replace(".cu", ".o")), [])
-         for s in ("api.cu", "sh.cu", "graph.cu", "coo.cu")]
+         for s in ("api.cu", "sh.cu", "graph.cu", "coo.cu", "radial.cu")]
     for i in config_ids():
-        for part in (0, 1, 2, 3, 4):   # forward, backward, double backward (plain, pipelined), narrow forward
+        # forward, backward, double backward (plain, pipelined), narrow forward, radial conv
+        for part in (0, 1, 2, 3, 4, 5):
             u.append((os.path.join(CSRC, "instances.cu"), os.path.join(OBJDIR, f"cfg{i}_{part}.o"),
                       [f"-DE3GB_CFG={i}", f"-DE3GB_PART={part}"]))
     return u

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -13,6 +14,7 @@
 
 #include "../../include/e3gb.h"
 #include "kernels.cuh"
+#include "radial.cuh"
 
 namespace e3gb {
 #define E3GB_CONFIG(ID, XC, L2, L3, PP) const ConfigOps* ops_##ID();
@@ -28,9 +30,11 @@ constexpr int kNumConfigs = int(sizeof(kRegistry) / sizeof(kRegistry[0]));
 
 cudaError_t sh_forward(int lmax, int64_t n, const float* vec, void* y, int bf16, cudaStream_t s);
 cudaError_t sh_backward(int lmax, int64_t n, const float* vec, const void* dy, float* dvec, int bf16, cudaStream_t s);
-size_t graph_workspace_bytes(int64_t N);
+size_t graph_workspace_bytes(int64_t N, int64_t E);
+int64_t graph_static_tiles_cap(size_t scratch_ints);
 cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
-                          int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s);
+                          int32_t* csc_edge, int32_t* csc_recv, void* ws, int64_t tiles_cap, unsigned* err,
+                          cudaStream_t s);
 size_t coo_smem_bytes(bool backward, int d1, int d2, int D, int P, int Nq);
 template <class T>
 cudaError_t coo_tp(bool backward, int64_t R, int d1, int d2, int D, int P, int Nq, int nrec, const int32_t* rec,
@@ -43,20 +47,20 @@ cudaError_t zero_padding_edges(int64_t N, int64_t E, const int32_t* csc_ptr, con
 // ------------------------------------------------------------------------------------------
 // launch sizing: grid = min(blocks needed, resident blocks per SM x SMs), cached per kernel
 // ------------------------------------------------------------------------------------------
-int grid_for(const void* kernel, int block, int64_t per_block, int64_t units) {
+int grid_for(const void* kernel, int block, int64_t per_block, int64_t units, int smem) {
     if (units <= 0) return 0;
     static std::mutex mu;
-    static std::map<std::pair<const void*, int>, int> resident;  // blocks per device, by kernel
+    static std::map<std::tuple<const void*, int, int>, int> resident;  // blocks per device, by kernel and smem
     int dev = 0;
     cudaGetDevice(&dev);
     int cap = 0;
     {
         std::lock_guard<std::mutex> lk(mu);
-        const std::pair<const void*, int> key(kernel, dev);
+        const std::tuple<const void*, int, int> key(kernel, dev, smem);
         auto it = resident.find(key);
         if (it == resident.end()) {
             int per_sm = 0, sms = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, 0);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, size_t(smem));
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             cap = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
             resident.emplace(key, cap);
@@ -307,8 +311,8 @@ e3gb_status e3gb_tp_backward(const e3gb_table* t, int64_t rows, const void* x, c
                        "tp_backward launch");
 }
 
-size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes) {
-    return n_nodes < 0 ? 0 : graph_workspace_bytes(n_nodes);
+size_t e3gb_graph_prepare_workspace_bytes(int64_t n_nodes, int64_t n_edges) {
+    return (n_nodes < 0 || n_edges < 0) ? 0 : graph_workspace_bytes(n_nodes, n_edges);
 }
 
 e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* rowptr, const int32_t* sender,
@@ -317,8 +321,9 @@ e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* 
     if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
     if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
     if (n_nodes == 0 && n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
-    if (ws_bytes < graph_workspace_bytes(n_nodes))
-        return fail(E3GB_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, graph_workspace_bytes(n_nodes));
+    if (ws_bytes < graph_workspace_bytes(n_nodes, n_edges))
+        return fail(E3GB_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes,
+                    graph_workspace_bytes(n_nodes, n_edges));
     E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
     E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
     E3GB_TRY(check_ptr(workspace, "workspace", 16, true));
@@ -328,16 +333,16 @@ e3gb_status e3gb_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* 
     e3gb_status st = E3GB_OK;
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;
-    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, workspace, err,
-                                     (cudaStream_t)stream),
+    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, workspace, 0,
+                                     err, (cudaStream_t)stream),
                        "graph_prepare launch");
 }
 
 // Allocation-free variant of e3gb_graph_prepare (see the header for who needs it): the
-// per-node counters live in this file-scope array. Host code must not pass the symbol
-// itself to a kernel (in host code it names a host-side stand-in); the device address is
-// looked up once per device with cudaGetSymbolAddress and passed on.
-static __device__ __align__(256) int32_t e3gb_prepare_scratch[E3GB_STATIC_PREPARE_MAX_NODES + 1];
+// sort's per-tile digit counts live in this file-scope array. Host code must not pass the
+// symbol itself to a kernel (in host code it names a host-side stand-in); the device address
+// is looked up once per device with cudaGetSymbolAddress and passed on.
+static __device__ __align__(256) int32_t e3gb_prepare_scratch[E3GB_STATIC_PREPARE_SCRATCH_BYTES / 4];
 
 static int32_t* prepare_scratch(e3gb_status* st) {
     static std::mutex mu;
@@ -364,12 +369,8 @@ static int32_t* prepare_scratch(e3gb_status* st) {
 e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const int32_t* rowptr, const int32_t* sender,
                                       int32_t* csc_ptr, int32_t* csc_edge, int32_t* csc_recv, void* stream) {
     if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
-    if (n_nodes > E3GB_STATIC_PREPARE_MAX_NODES)
-        return fail(E3GB_ERR_INVALID_ARG,
-                    "n_nodes %lld exceeds the static scratch of e3gb_graph_prepare_static (at most %d nodes); "
-                    "use e3gb_graph_prepare with a workspace",
-                    (long long)n_nodes, E3GB_STATIC_PREPARE_MAX_NODES);
-    if (n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "n_edges must be < 2^31-1");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX)
+        return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1 (e3gb_graph_prepare_static)");
     if (n_nodes == 0 && n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
     E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
     E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
@@ -381,9 +382,11 @@ e3gb_status e3gb_graph_prepare_static(int64_t n_nodes, int64_t n_edges, const in
     if (err == nullptr) return st;
     int32_t* scratch = prepare_scratch(&st);
     if (scratch == nullptr) return st;
-    // the shared graph_prepare path zeroes the counters on the stream before using them
-    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, scratch, err,
-                                     (cudaStream_t)stream),
+    // the tile count is capped so that the counts fit the array; every count is written
+    // before it is read, so the previous call's contents need no clearing
+    static const int64_t cap = graph_static_tiles_cap(E3GB_STATIC_PREPARE_SCRATCH_BYTES / 4);
+    return cuda_status(graph_prepare(n_nodes, n_edges, rowptr, sender, csc_ptr, csc_edge, csc_recv, scratch, cap,
+                                     err, (cudaStream_t)stream),
                        "graph_prepare_static launch");
 }
 
@@ -448,6 +451,115 @@ e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_e
                          "conv_backward launch"));
     return cuda_status(zero_padding_edges(n_nodes, n_edges, csc_ptr, csc_edge, csc_recv, pad_node, (float*)dw,
                                           int64_t(t->ops->NP) * t->mul, (float*)dy, t->ops->D2, (cudaStream_t)stream),
+                       "zero_padding_edges launch");
+}
+
+// ------------------------------------------------------------------------------------------
+// radial edge scalars and the radial convolution
+// ------------------------------------------------------------------------------------------
+static e3gb_status check_radial_net(int32_t n_basis, int32_t hidden, float r_cut) {
+    if (n_basis < 1 || n_basis > kRadialMaxBasis)
+        return fail(E3GB_ERR_INVALID_ARG, "n_basis %d outside [1, %d]", n_basis, kRadialMaxBasis);
+    if (hidden < 1 || hidden > kRadialMaxHidden)
+        return fail(E3GB_ERR_INVALID_ARG, "hidden %d outside [1, %d]", hidden, kRadialMaxHidden);
+    if (!(r_cut > 0.f)) return fail(E3GB_ERR_INVALID_ARG, "r_cut must be positive");
+    return E3GB_OK;
+}
+
+e3gb_status e3gb_radial_hidden(int64_t n_edges, const float* vec, const float* W1, int32_t n_basis, int32_t hidden,
+                               float r_cut, float* h, void* stream) {
+    if (n_edges < 0 || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "n_edges outside [0, 2^31-1)");
+    E3GB_TRY(check_radial_net(n_basis, hidden, r_cut));
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(vec, "vec", 4, edges));
+    E3GB_TRY(check_ptr(W1, "W1", 4, true));
+    E3GB_TRY(check_ptr(h, "h", 4, edges));
+    return cuda_status(radial_hidden(n_edges, vec, W1, n_basis, hidden, r_cut, h, (cudaStream_t)stream),
+                       "radial_hidden launch");
+}
+
+e3gb_status e3gb_radial_backward(int64_t n_edges, const float* vec, const float* W1, int32_t n_basis, int32_t hidden,
+                                 float r_cut, const float* dh, float* dvec, int32_t accumulate, void* stream) {
+    if (n_edges < 0 || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "n_edges outside [0, 2^31-1)");
+    E3GB_TRY(check_radial_net(n_basis, hidden, r_cut));
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(vec, "vec", 4, edges));
+    E3GB_TRY(check_ptr(W1, "W1", 4, true));
+    E3GB_TRY(check_ptr(dh, "dh", 4, edges));
+    E3GB_TRY(check_ptr(dvec, "dvec", 4, edges));
+    return cuda_status(radial_backward(n_edges, vec, W1, n_basis, hidden, r_cut, dh, dvec, accumulate ? 1 : 0,
+                                       (cudaStream_t)stream),
+                       "radial_backward launch");
+}
+
+static e3gb_status check_radial_conv(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, int32_t hidden,
+                                     int64_t pad_node, e3gb_dtype dtype) {
+    E3GB_TRY(check_table(t, dtype));
+    if (dtype != E3GB_F32) return fail(E3GB_ERR_UNSUPPORTED, "the radial convolution is built for fp32 only");
+    if (hidden != kRadialHidden)
+        return fail(E3GB_ERR_UNSUPPORTED, "the radial convolution is built for hidden = %d (got %d)", kRadialHidden,
+                    hidden);
+    if (t->ops->conv_fwd_rad == nullptr || int64_t(kRadialHidden) * t->ops->NP * t->mul * 4 > 232448)
+        return fail(E3GB_ERR_UNSUPPORTED, "W2 of %d x %d x %d floats does not fit in shared memory", kRadialHidden,
+                    t->ops->NP, t->mul);
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (pad_node < -1 || pad_node >= n_nodes)
+        return fail(E3GB_ERR_INVALID_ARG, "pad_node %lld outside [-1, n_nodes)", (long long)pad_node);
+    if (n_nodes == 0 && n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+    return E3GB_OK;
+}
+
+e3gb_status e3gb_conv_forward_radial(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
+                                     const int32_t* sender, const void* x, const void* y, const float* h,
+                                     const float* W2, int32_t hidden, float scale, int64_t pad_node, void* m,
+                                     e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_radial_conv(t, n_nodes, n_edges, hidden, pad_node, dtype));
+    if (n_nodes == 0) return ok();
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", 16, true));
+    E3GB_TRY(check_ptr(y, "y", 4, edges));
+    E3GB_TRY(check_ptr(h, "h", 16, edges));
+    E3GB_TRY(check_ptr(W2, "W2", 16, true));
+    E3GB_TRY(check_ptr(m, "m", 16, true));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    return cuda_status(t->ops->conv_fwd_rad(n_nodes, n_edges, t->mul, rowptr, sender, (const float*)x, (const float*)y,
+                                            h, W2, scale, (float*)m, pad_node, err, (cudaStream_t)stream),
+                       "conv_forward_radial launch");
+}
+
+e3gb_status e3gb_conv_backward_radial(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* csc_ptr,
+                                      const int32_t* csc_edge, const int32_t* csc_recv, const void* x, const void* y,
+                                      const float* h, const float* W2, int32_t hidden, const void* dm, float scale,
+                                      int64_t pad_node, void* dx, void* dy, float* dh, e3gb_dtype dtype,
+                                      void* stream) {
+    E3GB_TRY(check_radial_conv(t, n_nodes, n_edges, hidden, pad_node, dtype));
+    if (n_nodes == 0) return ok();
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(csc_ptr, "csc_ptr", 4, true));
+    E3GB_TRY(check_ptr(csc_edge, "csc_edge", 4, edges));
+    E3GB_TRY(check_ptr(csc_recv, "csc_recv", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", 16, true));
+    E3GB_TRY(check_ptr(y, "y", 4, edges));
+    E3GB_TRY(check_ptr(h, "h", 16, edges));
+    E3GB_TRY(check_ptr(W2, "W2", 16, true));
+    E3GB_TRY(check_ptr(dm, "dm", 16, true));
+    E3GB_TRY(check_ptr(dx, "dx", 16, true));
+    E3GB_TRY(check_ptr(dy, "dy", 4, edges));
+    E3GB_TRY(check_ptr(dh, "dh", 16, edges));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    E3GB_TRY(cuda_status(t->ops->conv_bwd_rad(n_nodes, n_edges, t->mul, csc_ptr, csc_edge, csc_recv, (const float*)x,
+                                              (const float*)y, h, W2, (const float*)dm, scale, (float*)dx, (float*)dy,
+                                              dh, pad_node, err, (cudaStream_t)stream),
+                         "conv_backward_radial launch"));
+    return cuda_status(zero_padding_edges(n_nodes, n_edges, csc_ptr, csc_edge, csc_recv, pad_node, dh, kRadialHidden,
+                                          (float*)dy, t->ops->D2, (cudaStream_t)stream),
                        "zero_padding_edges launch");
 }
 

@@ -287,28 +287,48 @@ __device__ __forceinline__ float warp_sum_transposed(float (&v)[N], int lane, in
 // ------------------------------------------------------------------------------------------
 // forward
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T, int NSLOT>
+// RH > 0 (the radial form): no w rows are streamed; the edge's item also carries its RH hidden
+// activations h[e], and each path's weights are formed in registers from the block's shared
+// copy of the output layer W2 [RH][NP][128]: w_p = sum_k h_k W2[k][p].
+template <class Cfg, class T, int NSLOT, int RH = 0>
 struct FwdPipe {
     using PP = PipePlan<Cfg>;
-    static constexpr int NCH = 1 + PP::NWC;                       // items per edge
+    static constexpr int NCH = RH > 0 ? 1 : 1 + PP::NWC;          // items per edge
     static constexpr int ROWB = kPipeNq * sizeof(T);              // bytes of one 128-channel row
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
-    static constexpr int ROWS = Cfg::D1 > PP::PPC ? Cfg::D1 : PP::PPC;
-    static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
+    static constexpr int HB = RH * 4;                             // the edge's hidden activations (fp32)
+    static constexpr int ROWS = RH > 0 ? Cfg::D1 : (Cfg::D1 > PP::PPC ? Cfg::D1 : PP::PPC);
+    static constexpr int SLOT = ((ROWS * ROWB + YB + HB) + 127) / 128 * 128;
     static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 4;
+    static constexpr int W2B = RH * Cfg::NP * kPipeNq * 4;        // shared copy of W2, ahead of the warps
 };
 
-template <class Cfg, class T, int NSLOT, int WARPS>
+// w_p = sum_k h_k W2[k][p] for the lane's four channels
+template <class Cfg, int RH>
+__device__ __forceinline__ Q2 radial_w(const float* __restrict__ w2s, const float (&hv)[RH], int p, int c0) {
+    Q2 wv = q2_zero();
+#pragma unroll
+    for (int k = 0; k < RH; ++k) {
+        const float2 hh = make_float2(hv[k], hv[k]);
+        wv = q2_fma(hh, lds_q2<float>(w2s + (k * Cfg::NP + p) * kPipeNq + c0), wv);
+    }
+    return wv;
+}
+
+template <class Cfg, class T, int NSLOT, int WARPS, int RH = 0>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ sender,
                          const T* __restrict__ x, const T* __restrict__ y, const T* __restrict__ w, float scale,
-                         float* __restrict__ m, int64_t pad, unsigned* __restrict__ err) {
-    using F = FwdPipe<Cfg, T, NSLOT>;
+                         float* __restrict__ m, int64_t pad, unsigned* __restrict__ err,
+                         const float* __restrict__ hrad = nullptr, const float* __restrict__ W2 = nullptr) {
+    using F = FwdPipe<Cfg, T, NSLOT, RH>;
     using PP = PipePlan<Cfg>;
     extern __shared__ __align__(128) unsigned char smem[];
+    const float* w2s = reinterpret_cast<const float*>(smem);
+    if constexpr (RH > 0) load_w2_shared(reinterpret_cast<float*>(smem), W2, RH * Cfg::NP * kPipeNq);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    unsigned char* wsm = smem + wid * F::WARP_BYTES;
+    unsigned char* wsm = smem + F::W2B + wid * F::WARP_BYTES;
     float2* sA = reinterpret_cast<float2*>(wsm + NSLOT * F::SLOT);
     const int c0 = lane * kVec;
     const int64_t gw = int64_t(blockIdx.x) * WARPS + wid;
@@ -345,6 +365,9 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
                 }
                 if (lane < F::YB / 16) cp_async16(slot + Cfg::D1 * F::ROWB + lane * 16,
                                                    reinterpret_cast<const unsigned char*>(y + pe * Cfg::D2) + lane * 16);
+                if constexpr (RH > 0)
+                    if (lane < F::HB / 16)
+                        cp_async16(slot + Cfg::D1 * F::ROWB + F::YB + lane * 16, hrad + pe * RH + lane * 4);
             } else {
                 const int p0 = (pc - 1) * PP::PPC;
                 const int np = (Cfg::NP - p0) < PP::PPC ? (Cfg::NP - p0) : PP::PPC;
@@ -395,6 +418,17 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
                     for (int r = 0; r < Cfg::D1; ++r)
                         xv[r] = ok ? lds_q2<T>(reinterpret_cast<const T*>(slot + r * F::ROWB) + c0) : q2_zero();
                     __syncwarp();   // A visible to every lane
+                    if constexpr (RH > 0) {
+                        float hv[RH];
+                        const float* sh = reinterpret_cast<const float*>(slot + Cfg::D1 * F::ROWB + F::YB);
+#pragma unroll
+                        for (int k = 0; k < RH; ++k) hv[k] = sh[k];
+                        sfor<Cfg::NP>([&](auto pp) {
+                            constexpr int p = decltype(pp)::value;
+                            fwd_path<Cfg, p>(sA, xv, radial_w<Cfg, RH>(w2s, hv, p, c0), acc);
+                        });
+                        __syncwarp();   // A is rebuilt for the next edge
+                    }
                 } else {
                     constexpr int p0 = (ch - 1) * PP::PPC;
                     constexpr int np = (Cfg::NP - p0) < PP::PPC ? (Cfg::NP - p0) : PP::PPC;
@@ -421,26 +455,45 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
 // ------------------------------------------------------------------------------------------
 // backward (sender order)
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T, int NSLOT>
+// RH > 0 (the radial form): block items carry only the dm rows; the edge's first item also
+// carries its hidden activations h[e]; w_p is formed from the shared copy of W2 and the
+// cotangent dh[e][k] = sum_p sum_c W2[k][p][c] dw_p[c] replaces the dw row.
+template <class Cfg, class T, int NSLOT, int RH = 0>
 struct BwdPipe {
     using PP = PipePlan<Cfg>;
     static constexpr int ROWB = kPipeNq * sizeof(T);
     static constexpr int YB = ((Cfg::D2 * sizeof(T) + 15) / 16) * 16;
-    static constexpr int ROWS = Cfg::D1 > PP::max_block_rows ? Cfg::D1 : PP::max_block_rows;
-    static constexpr int SLOT = ((ROWS * ROWB + YB) + 127) / 128 * 128;
+    static constexpr int HB = RH * 4;
+    static constexpr int max_out_rows = [] {
+        int r = 0;
+        for (int j = 0; j < Cfg::NOUT; ++j) r = 2 * Cfg::table.outs[j].l + 1 > r ? 2 * Cfg::table.outs[j].l + 1 : r;
+        return r;
+    }();
+    static constexpr int BROWS = RH > 0 ? max_out_rows : PP::max_block_rows;
+    static constexpr int ROWS = Cfg::D1 > BROWS ? Cfg::D1 : BROWS;
+    static constexpr int SLOT = ((ROWS * ROWB + YB + HB) + 127) / 128 * 128;
     static constexpr int XBUF = Cfg::D1 * kPipeNq * 4;            // the sender's x rows (fp32)
     // the A buffer is given 8 bytes per entry although it uses 4: this layout measured ~3%
     // faster than the compact one on the 64k-atom workload
     static constexpr int WARP_BYTES = NSLOT * SLOT + PP::NAPAD * 8 + XBUF;
     static constexpr int NCH = Cfg::NOUT;   // items per edge (one per output block)
+    static constexpr int W2B = RH * Cfg::NP * kPipeNq * 4;
+};
+
+// radial backward's per-edge state: the hidden activations and the lane's partial dh
+template <int RH>
+struct RadEdge {
+    float h[RH > 0 ? RH : 1];
+    float dh[RH > 0 ? RH : 1];
+    const float* w2s;
 };
 
 // the part of an edge's backward that belongs to output block J; g rows from the slot
 // (the couplings in sA already carry the convolution scale; dy is scaled by the caller)
-template <class Cfg, class T, int J>
+template <class Cfg, class T, int J, int RH = 0>
 __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot, const float2* __restrict__ sA,
                                           const float* __restrict__ sx, Q2 (&dxa)[Cfg::D1], float (&dyp)[Cfg::D2],
-                                          float* __restrict__ dw_e, int c0) {
+                                          float* __restrict__ dw_e, int c0, RadEdge<RH>& rad) {
     using PP = PipePlan<Cfg>;
     constexpr int ROWB = kPipeNq * sizeof(T);
     constexpr int nrow = 2 * Cfg::table.outs[J].l + 1;
@@ -455,7 +508,9 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
         constexpr int na = Off<Cfg>::a[p + 1] - a0;
         constexpr int n1 = 2 * pi.l1 + 1;
         constexpr int base = PP::apos[p];
-        const Q2 wv = lds_q2<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0);
+        Q2 wv;
+        if constexpr (RH > 0) wv = radial_w<Cfg, RH>(rad.w2s, rad.h, p, c0);
+        else wv = lds_q2<T>(reinterpret_cast<const T*>(slot + (nrow + decltype(ii)::value) * ROWB) + c0);
         Q2 gp[n1], xw[n1], xr[n1];
 #pragma unroll
         for (int mm = 0; mm < n1; ++mm) {
@@ -489,25 +544,39 @@ __device__ __forceinline__ void bwd_block(const unsigned char* __restrict__ slot
             dwv = q2_fma(xr[mm], gp[mm], dwv);
             dxa[pi.xoff + mm] = q2_fma(wv, gp[mm], dxa[pi.xoff + mm]);
         }
-        __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0), make_float4(dwv.lo.x, dwv.lo.y, dwv.hi.x, dwv.hi.y));
+        if constexpr (RH > 0) {
+#pragma unroll
+            for (int k = 0; k < RH; ++k) {   // the lane's share of dh[k] = sum_c W2[k][p][c] dw_p[c]
+                const Q2 w2 = lds_q2<float>(rad.w2s + (k * Cfg::NP + p) * kPipeNq + c0);
+                const float2 s2 = __ffma2_rn(w2.hi, dwv.hi, __fmul2_rn(w2.lo, dwv.lo));
+                rad.dh[k] += s2.x + s2.y;
+            }
+        } else {
+            __stcs(reinterpret_cast<float4*>(dw_e + p * kPipeNq + c0),
+                   make_float4(dwv.lo.x, dwv.lo.y, dwv.hi.x, dwv.hi.y));
+        }
     });
 }
 
 // IDENT: the identity graph of the row-wise tensor product backward (App. E.1 Eq. (15)): row r
 // is a node with the single edge r from and to itself, scale 1; the index arrays are not read
 // and may be null, and so may err (no index can be out of range).
-template <class Cfg, class T, int NSLOT, int WARPS, bool IDENT = false>
+// RH > 0: the radial form (w unused; dw receives dh [E][RH]); not combined with IDENT.
+template <class Cfg, class T, int NSLOT, int WARPS, bool IDENT = false, int RH = 0>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr, const int32_t* __restrict__ cedge,
                           const int32_t* __restrict__ crecv, const T* __restrict__ x, const T* __restrict__ y,
                           const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
-                          float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err) {
-    using B = BwdPipe<Cfg, T, NSLOT>;
+                          float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err,
+                          const float* __restrict__ hrad = nullptr, const float* __restrict__ W2 = nullptr) {
+    static_assert(!(IDENT && RH > 0), "the identity graph has no radial form");
+    using B = BwdPipe<Cfg, T, NSLOT, RH>;
     using PP = PipePlan<Cfg>;
     extern __shared__ __align__(128) unsigned char smem[];
+    if constexpr (RH > 0) load_w2_shared(reinterpret_cast<float*>(smem), W2, RH * Cfg::NP * kPipeNq);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    unsigned char* wsm = smem + wid * B::WARP_BYTES;
+    unsigned char* wsm = smem + B::W2B + wid * B::WARP_BYTES;
     float2* sA = reinterpret_cast<float2*>(wsm + NSLOT * B::SLOT);
     float* sx = reinterpret_cast<float*>(wsm + NSLOT * B::SLOT + PP::NAPAD * 8);
     const int c0 = lane * kVec;
@@ -574,16 +643,21 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                             for (int r = 0; r < nrow; ++r)
                                 cp_async_slice<T>(slot + r * B::ROWB + c0 * sizeof(T),
                                                   dm + (bb * Cfg::D + zo + r) * kPipeNq + c0);
-                            sfor<PP::bpos[j + 1] - PP::bpos[j]>([&](auto ii) {
-                                constexpr int p = PP::bpath[PP::bpos[j] + decltype(ii)::value];
-                                cp_async_slice_hint<T>(slot + (nrow + decltype(ii)::value) * B::ROWB + c0 * sizeof(T),
-                                                  w + (e * Cfg::NP + p) * kPipeNq + c0, wpol);
-                            });
+                            if constexpr (RH == 0)
+                                sfor<PP::bpos[j + 1] - PP::bpos[j]>([&](auto ii) {
+                                    constexpr int p = PP::bpath[PP::bpos[j] + decltype(ii)::value];
+                                    cp_async_slice_hint<T>(
+                                        slot + (nrow + decltype(ii)::value) * B::ROWB + c0 * sizeof(T),
+                                        w + (e * Cfg::NP + p) * kPipeNq + c0, wpol);
+                                });
                         }
                     });
                     if (pc == 0 && lane < B::YB / 16)
                         cp_async16(slot + B::ROWS * B::ROWB + lane * 16,
                                    reinterpret_cast<const unsigned char*>(y + e * Cfg::D2) + lane * 16);
+                    if constexpr (RH > 0)
+                        if (pc == 0 && lane < B::HB / 16)
+                            cp_async16(slot + B::ROWS * B::ROWB + B::YB + lane * 16, hrad + e * RH + lane * 4);
                 }
                 if (++pc == B::NCH) {
                     pc = 0;
@@ -629,6 +703,12 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
 #pragma unroll
             for (int t = 0; t < Cfg::D2; ++t) dyp[t] = 0.f;
             float* dw_e = dw + (ok ? e : 0) * (Cfg::NP * kPipeNq);
+            RadEdge<RH> rad;
+            if constexpr (RH > 0) {
+                rad.w2s = reinterpret_cast<const float*>(smem);
+#pragma unroll
+                for (int k = 0; k < RH; ++k) rad.dh[k] = 0.f;
+            }
             sfor<B::NCH>([&](auto jj) {
                 constexpr int j = decltype(jj)::value;
                 issue(issued++);
@@ -640,14 +720,24 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
                     if (ok)
                         build_A_warp<Cfg, false, T>(reinterpret_cast<const T*>(slot + B::ROWS * B::ROWB), sA, lane,
                                                     scale);
+                    if constexpr (RH > 0) {
+                        const float* sh = reinterpret_cast<const float*>(slot + B::ROWS * B::ROWB + B::YB);
+#pragma unroll
+                        for (int k = 0; k < RH; ++k) rad.h[k] = sh[k];
+                    }
                     __syncwarp();
                 }
-                if (ok) bwd_block<Cfg, T, j>(slot, sA, sx, dxa, dyp, dw_e, c0);
+                if (ok) bwd_block<Cfg, T, j, RH>(slot, sA, sx, dxa, dyp, dw_e, c0, rad);
                 if constexpr (j == B::NCH - 1) __syncwarp();
             });
             int di = 0;
             const float dsum = warp_sum_transposed<Cfg::D2>(dyp, lane, &di);
             if (ok && (lane & (32 / Cfg::D2 - 1)) == 0) dy[e * Cfg::D2 + di] = dsum * scale;
+            if constexpr (RH > 0) {
+                int hi = 0;
+                const float hsum = warp_sum_transposed<RH>(rad.dh, lane, &hi);
+                if (ok && (lane & (32 / RH - 1)) == 0) dw[e * RH + hi] = hsum;
+            }
         }
 #pragma unroll
         for (int r = 0; r < Cfg::D1; ++r)
@@ -662,13 +752,16 @@ conv_backward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ cptr
 // ------------------------------------------------------------------------------------------
 constexpr int kSmemLimit = 232448;   // 227 KiB per block
 
-template <class Cfg, class T, bool BWD>
+template <class Cfg, class T, bool BWD, int RH = 0>
 struct PipeShape {
-    static constexpr int NSLOT = BWD ? 3 : 4;
-    static constexpr int WARP_BYTES = BWD ? BwdPipe<Cfg, T, NSLOT>::WARP_BYTES : FwdPipe<Cfg, T, NSLOT>::WARP_BYTES;
-    static constexpr int by_smem = kSmemLimit / WARP_BYTES;
+    // the radial form keeps a shared copy of W2 beside the warps' rings: fewer slots
+    static constexpr int NSLOT = BWD ? (RH > 0 ? 2 : 3) : (RH > 0 ? 3 : 4);
+    static constexpr int WARP_BYTES =
+        BWD ? BwdPipe<Cfg, T, NSLOT, RH>::WARP_BYTES : FwdPipe<Cfg, T, NSLOT, RH>::WARP_BYTES;
+    static constexpr int W2B = RH * Cfg::NP * kPipeNq * 4;
+    static constexpr int by_smem = (kSmemLimit - W2B) / WARP_BYTES;
     static constexpr int WARPS = by_smem < 8 ? by_smem : 8;
-    static constexpr int SMEM = WARPS * WARP_BYTES;
+    static constexpr int SMEM = W2B + WARPS * WARP_BYTES;
     static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4;
 };
 

@@ -4,14 +4,20 @@
 // the transposed graph: dx[a] sums over the edges whose sender is a. Walking the edges in
 // sender order lets one row group own dx[a] and sum it in registers in a fixed order, with
 // no atomics (the pages' TPU backward reduces dx keyed on senders for the same reason,
-// App. E.4 Alg. 7). Steps:
-//   1. count edges per sender (integer atomics: the counts do not depend on order);
-//   2. exclusive scan of the counts -> csc_ptr (one block);
-//   3. place each edge id into its sender's segment (any order);
-//   4. sort every segment by edge id (rank counting), which makes the index stable and
-//      deterministic;
-//   5. csc_recv[k] = receiver of csc_edge[k] (binary search in rowptr).
-// Workspace: the per-sender counters / cursors (n_nodes + 1 ints).
+// App. E.4 Alg. 7). The index is the edge ids stably sorted by sender, built in O(E) work
+// whatever the degree distribution (one padding node may send most of the edges):
+//   1. a least-significant-digit radix sort of the edge ids by key = sender, 8 bits per
+//      pass, ceil(bits(n_nodes) / 8) passes. Edges that belong to no receiver or have a
+//      sender outside [0, n_nodes) get the key n_nodes and sort to the end. Each pass splits
+//      the edges into tiles of T consecutive entries, one warp per tile: (a) per-tile digit
+//      counts, (b) an exclusive scan of the counts in digit-major order, (c) a stable scatter
+//      in which each warp walks its tile in order and ranks equal digits with a match mask.
+//      Keys are never stored: each pass gathers sender[edge id] again. The two output arrays
+//      csc_edge / csc_recv are the ping-pong buffers, and the last pass lands in csc_edge;
+//   2. csc_ptr[a] = first sorted position whose key is >= a (a binary search per node);
+//   3. csc_recv[k] = receiver of csc_edge[k] (binary search in rowptr); positions past the
+//      valid edges get -1 in both arrays.
+// Workspace: the per-tile digit counts (256 per tile) and the scan's block sums.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -20,98 +26,226 @@ namespace e3gb {
 
 namespace {
 constexpr unsigned kErrSender = 1u, kErrRowptr = 2u;
+constexpr int kRadixBits = 8, kBins = 1 << kRadixBits;
+constexpr int kScanBlock = 1024, kScanItems = 4;          // one scan block covers 4096 counts
+constexpr int64_t kScanChunk = int64_t(kScanBlock) * kScanItems;
+constexpr int kSortWarps = 8;                              // warps (tiles in flight) per sort block
 
-__global__ void count_kernel(int64_t N, int64_t E, const int32_t* __restrict__ sender, int32_t* __restrict__ cnt,
-                             unsigned* __restrict__ err) {
-    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < E; e += int64_t(gridDim.x) * blockDim.x) {
-        const int32_t s = sender[e];
-        if (s < 0 || s >= N) {
-            atomicOr(err, kErrSender);
-            continue;
-        }
-        atomicAdd(cnt + s, 1);
+// Which edges enter the index, and under which key.
+struct EdgeKeys {
+    int64_t N, E;
+    const int32_t* sender;
+    const int32_t* rowptr;
+
+    // key = sender for an edge inside [rowptr[0], rowptr[N]) with a sender in [0, N), else N
+    __device__ __forceinline__ int32_t key(int32_t e, int64_t lo, int64_t hi) const {
+        const int32_t s = __ldg(sender + e);
+        return (s >= 0 && s < N && e >= lo && e < hi) ? s : int32_t(N);
     }
+    __device__ __forceinline__ void range(int64_t& lo, int64_t& hi) const {
+        lo = __ldg(rowptr);
+        hi = __ldg(rowptr + N);
+        lo = lo < 0 ? 0 : lo;
+        hi = hi > E ? E : hi;
+    }
+};
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
 }
 
-// exclusive scan of cnt[0..N) into ptr[0..N], and cnt <- ptr[0..N) (the placement cursors)
-__global__ void __launch_bounds__(1024) scan_kernel(int64_t N, int32_t* __restrict__ cnt, int32_t* __restrict__ ptr) {
-    __shared__ int64_t part[1024];
-    const int t = threadIdx.x;
-    const int64_t chunk = (N + 1023) / 1024;
-    const int64_t lo = t * chunk, hi = (lo + chunk < N) ? lo + chunk : N;
-    int64_t s = 0;
-    for (int64_t i = lo; i < hi; ++i) s += cnt[i];
-    part[t] = s;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int64_t v = t >= off ? part[t - off] : 0;
-        __syncthreads();
-        part[t] += v;
-        __syncthreads();
-    }
-    int64_t run = t > 0 ? part[t - 1] : 0;   // exclusive prefix of this thread's chunk
-    for (int64_t i = lo; i < hi; ++i) {
-        const int32_t c = cnt[i];
-        ptr[i] = int32_t(run);
-        cnt[i] = int32_t(run);
-        run += c;
-    }
-    if (t == 1023) ptr[N] = int32_t(part[1023]);
-}
-
-__global__ void place_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr,
-                             const int32_t* __restrict__ sender, const int32_t* __restrict__ ptr,
-                             int32_t* __restrict__ cursor, int32_t* __restrict__ tmp,
-                             unsigned* __restrict__ err) {
-    for (int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; b < N; b += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t e0 = rowptr[b], e1 = rowptr[b + 1];
-        if (e0 < 0 || e1 < e0 || e1 > E) {
-            atomicOr(err, kErrRowptr);
-            continue;
-        }
-        for (int64_t e = e0; e < e1; ++e) {
-            const int32_t s = sender[e];
-            if (s < 0 || s >= N) continue;   // flagged by count_kernel
-            const int32_t pos = atomicAdd(cursor + s, 1);
-            if (pos >= ptr[s + 1]) {   // overlapping CSR segments: more placements than edges
-                atomicOr(err, kErrRowptr);
-                continue;
+// (a) per-tile digit counts: hist[d * n_tiles + tile]. Pass 0 reads the identity order
+// (in == nullptr) and flags out-of-range senders.
+__global__ void __launch_bounds__(32 * kSortWarps) radix_hist_kernel(EdgeKeys k, const int32_t* __restrict__ in,
+                                                                      int64_t T, int64_t n_tiles, int shift,
+                                                                      int32_t* __restrict__ hist,
+                                                                      unsigned* __restrict__ err) {
+    __shared__ int32_t cnt[kSortWarps][kBins];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    int64_t lo, hi;
+    k.range(lo, hi);
+    const int64_t nw = int64_t(gridDim.x) * kSortWarps;
+    for (int64_t tile = int64_t(blockIdx.x) * kSortWarps + wib; tile < n_tiles; tile += nw) {
+        for (int d = lane; d < kBins; d += 32) cnt[wib][d] = 0;
+        __syncwarp();
+        const int64_t b = tile * T, e = (b + T < k.E) ? b + T : k.E;
+        bool bad = false;
+        for (int64_t r = b; r < e; r += 32) {   // warp-uniform trip count
+            const int64_t i = r + lane;
+            int32_t d = -1;
+            if (i < e) {
+                const int32_t v = in ? in[i] : int32_t(i);
+                if (!in) {
+                    const int32_t s = __ldg(k.sender + v);
+                    bad |= (s < 0 || s >= k.N);
+                }
+                d = (k.key(v, lo, hi) >> shift) & (kBins - 1);
             }
-            tmp[pos] = int32_t(e);
+            // one shared-memory add per distinct digit of the round (a heavy sender makes
+            // whole rounds share one digit)
+            const unsigned peers = __match_any_sync(0xffffffffu, d);
+            if (d >= 0 && (peers & lanemask_lt()) == 0) cnt[wib][d] += __popc(peers);
+            __syncwarp();
+        }
+        if (bad) atomicOr(err, kErrSender);
+        __syncwarp();
+        for (int d = lane; d < kBins; d += 32) hist[int64_t(d) * n_tiles + tile] = cnt[wib][d];
+        __syncwarp();
+    }
+}
+
+// (c) stable scatter: out[off[d][tile] + (#earlier entries of the tile with digit d)] = v
+__global__ void __launch_bounds__(32 * kSortWarps) radix_scatter_kernel(EdgeKeys k, const int32_t* __restrict__ in,
+                                                                         int64_t T, int64_t n_tiles, int shift,
+                                                                         const int32_t* __restrict__ off,
+                                                                         int32_t* __restrict__ out) {
+    constexpr int kAhead = 4;   // rounds of 32 entries whose loads are issued together
+    __shared__ int32_t cur[kSortWarps][kBins];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const unsigned lt = lanemask_lt();
+    int64_t lo, hi;
+    k.range(lo, hi);
+    const int64_t nw = int64_t(gridDim.x) * kSortWarps;
+    for (int64_t tile = int64_t(blockIdx.x) * kSortWarps + wib; tile < n_tiles; tile += nw) {
+        for (int d = lane; d < kBins; d += 32) cur[wib][d] = off[int64_t(d) * n_tiles + tile];
+        __syncwarp();
+        const int64_t b = tile * T, e = (b + T < k.E) ? b + T : k.E;
+        for (int64_t r0 = b; r0 < e; r0 += 32 * kAhead) {
+            int32_t v[kAhead], dg[kAhead];
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j) {
+                const int64_t i = r0 + 32 * j + lane;
+                v[j] = i < e ? (in ? in[i] : int32_t(i)) : -1;
+            }
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j)
+                dg[j] = v[j] >= 0 ? (k.key(v[j], lo, hi) >> shift) & (kBins - 1) : -1;
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j) {
+                const unsigned peers = __match_any_sync(0xffffffffu, dg[j]);
+                int32_t base = 0;
+                if (dg[j] >= 0) base = cur[wib][dg[j]];
+                __syncwarp();
+                if (dg[j] >= 0) {
+                    out[base + __popc(peers & lt)] = v[j];
+                    if ((peers & lt) == 0) cur[wib][dg[j]] = base + __popc(peers);   // the group's first lane
+                }
+                __syncwarp();
+            }
         }
     }
 }
 
-// one block per sender segment: out[ptr[a] + rank(v)] = v, rank = #values smaller than v
-__global__ void rank_kernel(int64_t N, const int32_t* __restrict__ ptr, const int32_t* __restrict__ cursor,
-                            const int32_t* __restrict__ tmp, int32_t* __restrict__ out) {
-    for (int64_t a = blockIdx.x; a < N; a += gridDim.x) {
-        const int64_t s = ptr[a];
-        const int64_t cap = int64_t(ptr[a + 1]) - s;
-        // edges of a rejected receiver segment never arrive: the cursor says how many did
-        int64_t n = int64_t(cursor[a]) - s;
-        n = n < cap ? n : cap;
-        // slots that no valid edge fills stay marked invalid (-1)
-        for (int64_t i = threadIdx.x; i < cap; i += blockDim.x) out[s + i] = -1;
-        __syncthreads();
-        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-            const int32_t v = tmp[s + i];
-            int64_t r = 0;
-            for (int64_t j = 0; j < n; ++j) r += tmp[s + j] < v;
-            out[s + r] = v;
+// block-wide exclusive scan of one value per thread (blockDim.x == kScanBlock); returns the
+// thread's exclusive prefix and sets *total
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
+    __shared__ int64_t warp_sums[kScanBlock / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int64_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
         }
-        __syncthreads();
+        warp_sums[lane] = s;   // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = wid > 0 ? warp_sums[wid - 1] : 0;
+    *total = warp_sums[kScanBlock / 32 - 1];
+    __syncthreads();   // warp_sums is reused by the next call
+    return before + incl - v;
+}
+
+// (b) exclusive scan of a[0..n) in place, three launches: block sums, a scan of the block
+// sums, then each block's scan plus its offset.
+__global__ void __launch_bounds__(kScanBlock) scan_sums_kernel(const int32_t* __restrict__ a, int64_t n,
+                                                               int32_t* __restrict__ sums) {
+    const int64_t b = int64_t(blockIdx.x) * kScanChunk;
+    int64_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+        const int64_t i = b + int64_t(j) * kScanBlock + threadIdx.x;
+        if (i < n) s += a[i];
+    }
+    int64_t total;
+    block_exclusive_scan(s, &total);
+    if (threadIdx.x == 0) sums[blockIdx.x] = int32_t(total);
+}
+
+__global__ void __launch_bounds__(kScanBlock) scan_top_kernel(int32_t* __restrict__ sums, int64_t n) {
+    int64_t carry = 0;
+    for (int64_t b = 0; b < n; b += kScanBlock) {
+        const int64_t i = b + threadIdx.x;
+        const int64_t v = i < n ? sums[i] : 0;
+        int64_t total;
+        const int64_t ex = block_exclusive_scan(v, &total);
+        if (i < n) sums[i] = int32_t(carry + ex);
+        carry += total;
     }
 }
 
-__global__ void recv_kernel(int64_t N, int64_t K, const int32_t* __restrict__ rowptr,
-                            const int32_t* __restrict__ edge, int32_t* __restrict__ recv) {
-    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < K; k += int64_t(gridDim.x) * blockDim.x) {
-        const int32_t e = edge[k];
-        if (e < 0) {
+__global__ void __launch_bounds__(kScanBlock) scan_apply_kernel(int32_t* __restrict__ a, int64_t n,
+                                                                const int32_t* __restrict__ sums) {
+    const int64_t b = int64_t(blockIdx.x) * kScanChunk + int64_t(threadIdx.x) * kScanItems;
+    int32_t v[kScanItems];
+    int64_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+        v[j] = b + j < n ? a[b + j] : 0;
+        s += v[j];
+    }
+    int64_t total;
+    int64_t run = block_exclusive_scan(s, &total) + sums[blockIdx.x];
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+        if (b + j < n) a[b + j] = int32_t(run);
+        run += v[j];
+    }
+}
+
+// csc_ptr[a] = first position of the sorted edge ids whose key is >= a, a in [0, N]; also
+// checks every receiver segment of rowptr
+__global__ void ptr_kernel(EdgeKeys k, const int32_t* __restrict__ sorted, int32_t* __restrict__ ptr,
+                           unsigned* __restrict__ err) {
+    int64_t lo, hi;
+    k.range(lo, hi);
+    for (int64_t a = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; a <= k.N; a += int64_t(gridDim.x) * blockDim.x) {
+        if (a < k.N) {
+            const int64_t e0 = k.rowptr[a], e1 = k.rowptr[a + 1];
+            if (e0 < 0 || e1 < e0 || e1 > k.E) atomicOr(err, kErrRowptr);
+        }
+        int64_t l = 0, h = k.E;   // invariant: key(sorted[l-1]) < a <= key(sorted[h])
+        while (l < h) {
+            const int64_t mid = (l + h) >> 1;
+            if (k.key(sorted[mid], lo, hi) < a) l = mid + 1; else h = mid;
+        }
+        ptr[a] = int32_t(l);
+    }
+}
+
+// csc_recv[k] = receiver of csc_edge[k]; entries past csc_ptr[N] (edges left out) become -1
+__global__ void recv_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr,
+                            const int32_t* __restrict__ ptr, int32_t* __restrict__ edge,
+                            int32_t* __restrict__ recv) {
+    const int64_t n_valid = ptr[N];
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < E; k += int64_t(gridDim.x) * blockDim.x) {
+        if (k >= n_valid) {
+            edge[k] = -1;
             recv[k] = -1;
             continue;
         }
+        const int32_t e = edge[k];
         // largest b with rowptr[b] <= e
         int64_t lo = 0, hi = N;   // invariant: rowptr[lo] <= e < rowptr[hi]
         while (hi - lo > 1) {
@@ -174,21 +308,68 @@ cudaError_t zero_padding_edges(int64_t N, int64_t E, const int32_t* csc_ptr, con
     return cudaGetLastError();
 }
 
-size_t graph_workspace_bytes(int64_t N) { return size_t((N + 1) * 4 + 255) / 256 * 256; }
+// Tile length (entries per warp) of the sort; tiles_cap > 0 bounds the tile count so that
+// the counts fit a fixed scratch (the tile then grows with the edge count).
+int64_t sort_tile(int64_t E, int64_t tiles_cap) {
+    int64_t T = 1024;
+    if (tiles_cap > 0)
+        while ((E + T - 1) / T > tiles_cap) T *= 2;
+    return T;
+}
+
+size_t scan_sums_count(int64_t n) { return size_t((n + kScanChunk - 1) / kScanChunk); }
+
+// int32 entries of the sort's scratch for tile length T: the digit counts, then the scan's block sums
+size_t graph_scratch_ints(int64_t E, int64_t T) {
+    const int64_t n_hist = int64_t(kBins) * ((E + T - 1) / T);
+    return size_t(n_hist) + scan_sums_count(n_hist) + 1;
+}
+
+int64_t graph_static_tiles_cap(size_t scratch_ints) {
+    // largest tile count whose counts and block sums fit
+    int64_t t = int64_t(scratch_ints) / kBins;
+    while (t > 0 && graph_scratch_ints(t * 1024, 1024) > scratch_ints) --t;
+    return t;
+}
+
+size_t graph_workspace_bytes(int64_t N, int64_t E) {
+    (void)N;
+    return (graph_scratch_ints(E, sort_tile(E, 0)) * 4 + 255) / 256 * 256;
+}
 
 cudaError_t graph_prepare(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, int32_t* csc_ptr,
-                          int32_t* csc_edge, int32_t* csc_recv, void* ws, unsigned* err, cudaStream_t s) {
-    int32_t* cnt = static_cast<int32_t*>(ws);
-    cudaError_t st = cudaMemsetAsync(cnt, 0, size_t(N + 1) * 4, s);
-    if (st != cudaSuccess) return st;
-    if (E > 0) count_kernel<<<grid1d(E, 256, 4096), 256, 0, s>>>(N, E, sender, cnt, err);
-    scan_kernel<<<1, 1024, 0, s>>>(N, cnt, csc_ptr);
+                          int32_t* csc_edge, int32_t* csc_recv, void* ws, int64_t tiles_cap, unsigned* err,
+                          cudaStream_t s) {
+    const EdgeKeys k{N, E, sender, rowptr};
     if (E > 0) {
-        // csc_recv is the temporary for unsorted segments; it is overwritten in step 5
-        place_kernel<<<grid1d(N, 256, 4096), 256, 0, s>>>(N, E, rowptr, sender, csc_ptr, cnt, csc_recv, err);
-        rank_kernel<<<int(N < 65535 ? (N > 0 ? N : 1) : 65535), 64, 0, s>>>(N, csc_ptr, cnt, csc_recv, csc_edge);
-        recv_kernel<<<grid1d(E, 256, 4096), 256, 0, s>>>(N, E, rowptr, csc_edge, csc_recv);
+        int dev = 0, sms = 0;
+        cudaError_t st = cudaGetDevice(&dev);
+        if (st == cudaSuccess) st = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (st != cudaSuccess) return st;
+        const int64_t T = sort_tile(E, tiles_cap);
+        const int64_t n_tiles = (E + T - 1) / T;
+        const int64_t n_hist = int64_t(kBins) * n_tiles;
+        int32_t* hist = static_cast<int32_t*>(ws);
+        int32_t* sums = hist + n_hist;
+        const int64_t n_sums = int64_t(scan_sums_count(n_hist));
+        int bits = 0;
+        while ((int64_t(1) << bits) <= N) ++bits;   // keys lie in [0, N]
+        const int passes = bits > kRadixBits ? (bits + kRadixBits - 1) / kRadixBits : 1;
+        const int sort_grid = grid1d((n_tiles + kSortWarps - 1) / kSortWarps, 1, sms * 16);
+        const int32_t* in = nullptr;
+        for (int p = 0; p < passes; ++p) {
+            int32_t* out = ((passes - 1 - p) % 2 == 0) ? csc_edge : csc_recv;
+            const int shift = p * kRadixBits;
+            radix_hist_kernel<<<sort_grid, 32 * kSortWarps, 0, s>>>(k, in, T, n_tiles, shift, hist, err);
+            scan_sums_kernel<<<int(n_sums), kScanBlock, 0, s>>>(hist, n_hist, sums);
+            scan_top_kernel<<<1, kScanBlock, 0, s>>>(sums, n_sums);
+            scan_apply_kernel<<<int(n_sums), kScanBlock, 0, s>>>(hist, n_hist, sums);
+            radix_scatter_kernel<<<sort_grid, 32 * kSortWarps, 0, s>>>(k, in, T, n_tiles, shift, hist, out);
+            in = out;
+        }
     }
+    ptr_kernel<<<grid1d(N + 1, 256, 4096), 256, 0, s>>>(k, csc_edge, csc_ptr, err);
+    if (E > 0) recv_kernel<<<grid1d(E, 256, 4096), 256, 0, s>>>(N, E, rowptr, csc_ptr, csc_edge, csc_recv);
     return cudaGetLastError();
 }
 

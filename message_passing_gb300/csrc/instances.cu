@@ -1,15 +1,16 @@
-// One irreps configuration's kernels and launchers; compiled five times per entry of configs.def,
+// One irreps configuration's kernels and launchers; compiled six times per entry of configs.def,
 // with -DE3GB_CFG=<id> -DE3GB_PART=0 (forward kernels and the ops table e3gb::ops_<id>())
 // -DE3GB_PART=1 (backward kernels), -DE3GB_PART=2 (double backward, plain kernels),
-// -DE3GB_PART=3 (double backward, 128-channel pipelined kernels) and -DE3GB_PART=4 (forward,
-// edge-slot kernels for 4-32 channels), so that the parts compile in parallel.
+// -DE3GB_PART=3 (double backward, 128-channel pipelined kernels), -DE3GB_PART=4 (forward,
+// edge-slot kernels for 4-32 channels) and -DE3GB_PART=5 (the radial convolution, forward and
+// backward), so that the parts compile in parallel.
 #include "conv_pipe.cuh"
 #include "conv_pipe_dd.cuh"
 #include "conv_slots.cuh"
 #include "kernels.cuh"
 
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
-#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3|4>"
+#error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3|4|5>"
 #endif
 #define E3GB_CAT2(a, b) a##b
 #define E3GB_CAT(a, b) E3GB_CAT2(a, b)
@@ -69,6 +70,15 @@ template <class T>
 bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, cudaStream_t s,
                     cudaError_t* st);
+// the radial convolution, fp32 (part 5): weights formed in the kernels from the hidden
+// activations h [E][kRadialHidden] and the output layer W2 [kRadialHidden][NP][Nq]
+cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const float* x,
+                         const float* y, const float* h, const float* W2, float scale, float* m, int64_t pad,
+                         unsigned* err, cudaStream_t s);
+cudaError_t conv_bwd_rad(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge,
+                         const int32_t* crecv, const float* x, const float* y, const float* h, const float* W2,
+                         const float* dm, float scale, float* dx, float* dy, float* dh, int64_t pad, unsigned* err,
+                         cudaStream_t s);
 // the pipelined double backward (part 3); returns false when the shape needs the plain kernels
 template <class T>
 bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const int32_t* cptr,
@@ -105,7 +115,7 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(R, R, nullptr, nullptr, nullptr, (const T*)x, (const T*)y,
                                                    (const T*)w, (const T*)dz, 1.f, (float*)dx, (float*)dy, (float*)dw,
-                                                   -1, nullptr);
+                                                   -1, nullptr, nullptr, nullptr);
             return cudaGetLastError();
         }
     }
@@ -134,7 +144,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale,
-                                                   (float*)m, pad, err);
+                                                   (float*)m, pad, err, nullptr, nullptr);
             return cudaGetLastError();
         }
     }
@@ -144,7 +154,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
-                              pad, err);
+                              pad, err, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -206,7 +216,8 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                                                   (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err);
+                                                   (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err,
+                                                   nullptr, nullptr);
             return cudaGetLastError();
         }
     }
@@ -214,7 +225,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, cptr, cedge, crecv, (const T*)x, (const T*)y, (const T*)w,
-                              (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err);
+                              (const T*)dm, scale, (float*)dx, (float*)dy, (float*)dw, pad, err, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -307,6 +318,65 @@ template bool conv_dbwd_pipe<__nv_bfloat16>(int64_t, int64_t, int, const int32_t
                                              const void*, const void*, const void*, const void*, float, void*, void*,
                                              void*, void*, int64_t, unsigned*, cudaStream_t, cudaError_t*);
 #endif  // part 3
+#if E3GB_PART == 5
+cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const float* x,
+                         const float* y, const float* h, const float* W2, float scale, float* m, int64_t pad,
+                         unsigned* err, cudaStream_t s) {
+    constexpr int RH = kRadialHidden;
+    using S = PipeShape<Cfg, float, false, RH>;
+    if constexpr (S::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(h) && aligned16(W2)) {
+            auto k = conv_forward_pipe_kernel<Cfg, float, S::NSLOT, S::WARPS, RH>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t need = (N + S::WARPS - 1) / S::WARPS;
+            const int grid = int(sm_count() < need ? sm_count() : need);
+            if (grid == 0) return cudaSuccess;
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, x, y, nullptr, scale, m, pad, err, h, W2);
+            return cudaGetLastError();
+        }
+    }
+    const int smem = RH * Cfg::NP * Nq * 4;
+    if (smem > kSmemLimit) return cudaErrorInvalidValue;
+    auto k = vec_for(Nq) == 4 ? conv_forward_kernel<Cfg, float, 4, RH> : conv_forward_kernel<Cfg, float, 1, RH>;
+    cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (st != cudaSuccess) return st;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N, smem);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, smem, s>>>(N, E, Nq, rowptr, sender, x, y, nullptr, scale, m, pad, err, h, W2);
+    return cudaGetLastError();
+}
+
+cudaError_t conv_bwd_rad(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge,
+                         const int32_t* crecv, const float* x, const float* y, const float* h, const float* W2,
+                         const float* dm, float scale, float* dx, float* dy, float* dh, int64_t pad, unsigned* err,
+                         cudaStream_t s) {
+    constexpr int RH = kRadialHidden;
+    using S = PipeShape<Cfg, float, true, RH>;
+    if constexpr (S::usable) {
+        if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(h) && aligned16(W2) && aligned16(dm)) {
+            auto k = conv_backward_pipe_kernel<Cfg, float, S::NSLOT, S::WARPS, false, RH>;
+            cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (st != cudaSuccess) return st;
+            const int64_t need = (N + S::WARPS - 1) / S::WARPS;
+            const int grid = int(sm_count() < need ? sm_count() : need);
+            if (grid == 0) return cudaSuccess;
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, cptr, cedge, crecv, x, y, nullptr, dm, scale, dx, dy, dh, pad,
+                                                   err, h, W2);
+            return cudaGetLastError();
+        }
+    }
+    const int smem = RH * Cfg::NP * Nq * 4;
+    if (smem > kSmemLimit) return cudaErrorInvalidValue;
+    auto k = vec_for(Nq) == 4 ? conv_backward_kernel<Cfg, float, 4, RH> : conv_backward_kernel<Cfg, float, 1, RH>;
+    cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (st != cudaSuccess) return st;
+    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N, smem);
+    if (grid == 0) return cudaSuccess;
+    k<<<grid, kBlock, smem, s>>>(N, E, Nq, cptr, cedge, crecv, x, y, nullptr, dm, scale, dx, dy, dh, pad, err, h, W2);
+    return cudaGetLastError();
+}
+#endif  // part 5
 }  // namespace cfg<id>
 
 #if E3GB_PART == 0
@@ -321,6 +391,8 @@ const ConfigOps kOps = {
     {conv_fwd<float>, conv_fwd<__nv_bfloat16>},
     {conv_bwd<float>, conv_bwd<__nv_bfloat16>},
     {conv_dbwd<float>, conv_dbwd<__nv_bfloat16>},
+    conv_fwd_rad,
+    conv_bwd_rad,
 };
 }  // namespace
 

@@ -246,6 +246,77 @@ __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, cons
 }
 
 // ------------------------------------------------------------------------------------------
+// Where the per-edge weights w[e][p][c] come from and where their cotangent dw goes.
+// WMem: rows of a w array in memory, dw rows written back.
+// WRad: the radial network's output layer evaluated in place (the fused edge-scalar producer:
+// "e3j ...", App. E.1 notation for s, App. A.3 "Linear mixing"),
+//   w[p][c] = sum_k h[k] W2[k][p][c],   dh[k] += sum_c W2[k][p][c] dw[p][c],
+// with W2 [RH][NP][Nq] in shared memory and h the edge's hidden activations; w and dw never
+// reach memory. dh holds the lane's partial sums over its own channels.
+// ------------------------------------------------------------------------------------------
+template <class T, int V>
+struct WMem {
+    const T* __restrict__ w_e;
+    float* __restrict__ dw_e;
+    int Nq, c0;
+    __device__ __forceinline__ void get(int p, float (&wv)[V]) const { loadv<T, V>(w_e + p * Nq + c0, wv); }
+    __device__ __forceinline__ void put(int p, const float (&dwv)[V]) { storev<V>(dw_e + p * Nq + c0, dwv); }
+};
+
+// V consecutive floats of a shared-memory row (plain loads: the read-only global path of
+// loadv must not be given a shared address)
+template <int V>
+__device__ __forceinline__ void lds_v(const float* p, float (&o)[V]) {
+    if constexpr (V == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    } else {
+#pragma unroll
+        for (int c = 0; c < V; ++c) o[c] = p[c];
+    }
+}
+
+template <int NP, int RH, int V>
+struct WRad {
+    const float* __restrict__ w2s;   // shared memory, [RH][NP][Nq]
+    float h[RH];
+    float dh[RH];
+    int Nq, c0;
+    __device__ __forceinline__ void get(int p, float (&wv)[V]) const {
+#pragma unroll
+        for (int c = 0; c < V; ++c) wv[c] = 0.f;
+#pragma unroll
+        for (int k = 0; k < RH; ++k) {
+            float w2[V];
+            lds_v<V>(w2s + (k * NP + p) * Nq + c0, w2);
+#pragma unroll
+            for (int c = 0; c < V; ++c) wv[c] = fmaf(h[k], w2[c], wv[c]);
+        }
+    }
+    __device__ __forceinline__ void put(int p, const float (&dwv)[V]) {
+#pragma unroll
+        for (int k = 0; k < RH; ++k) {
+            float w2[V];
+            lds_v<V>(w2s + (k * NP + p) * Nq + c0, w2);
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < V; ++c) s = fmaf(w2[c], dwv[c], s);
+            dh[k] += s;
+        }
+    }
+};
+
+// shared-memory copy of W2 [RH][NP][Nq] by the whole block (n floats; both ends 16-byte
+// aligned): 16-byte copies, then the n % 4 floats left over
+__device__ __forceinline__ void load_w2_shared(float* __restrict__ dst, const float* __restrict__ W2, int n) {
+    const int n4 = n & ~3;
+    for (int i = threadIdx.x * 4; i < n4; i += blockDim.x * 4)
+        *reinterpret_cast<float4*>(dst + i) = __ldg(reinterpret_cast<const float4*>(W2 + i));
+    for (int i = n4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(W2 + i);
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------------------------------
 // Backward body for one (row or edge) e: given x (of the row / sender), y[e], w[e] and the
 // cotangent rows g = scale * dz/dm (of the row / receiver), accumulate dx into dxa, the
 // lane's partial dy (summed over its channels) into dyp, and write dw[e].
@@ -254,10 +325,9 @@ __global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, cons
 //   dx[m1][q] += w[p][q] g_p[m1][q]
 //   dy[m2]    += sum_{records (m1,m2,m3,c)} c * sum_q x[m1][q] w[p][q] g[m3][q]
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T, int V>
-__device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][V], const float (&yv)[Cfg::D2],
-                                              const T* __restrict__ w_e, const T* __restrict__ g_row,
-                                              float gscale, float* __restrict__ dw_e, int Nq, int c0,
+template <class Cfg, class T, int V, class WS>
+__device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][V], const float (&yv)[Cfg::D2], WS& ws,
+                                              const T* __restrict__ g_row, float gscale, int Nq, int c0,
                                               float (&dxa)[Cfg::D1][V], float (&dyp)[Cfg::D2]) {
     sfor<Cfg::NOUT>([&](auto jj) {
         constexpr int j = decltype(jj)::value;
@@ -280,7 +350,7 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][V], con
                 float A[na];
                 build_A<Cfg, p>(yv, A);
                 float wv[V];
-                loadv<T, V>(w_e + p * Nq + c0, wv);
+                ws.get(p, wv);
                 float gp[n1][V];
                 float xw[n1][V];
 #pragma unroll
@@ -314,7 +384,7 @@ __device__ __forceinline__ void backward_body(const float (&xv)[Cfg::D1][V], con
                     }
                     dwv[c] = s;
                 }
-                storev<V>(dw_e + p * Nq + c0, dwv);
+                ws.put(p, dwv);
             }
         });
     });
@@ -359,9 +429,10 @@ __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, con
 #pragma unroll
             for (int c = 0; c < V; ++c) dxa[i][c] = 0.f;
         }
-        if (live)
-            backward_body<Cfg, T, V>(xv, yv, w + rr * Cfg::NP * Nq, dz + rr * Cfg::D * Nq, 1.f,
-                                  dw + rr * Cfg::NP * Nq, Nq, c0, dxa, dyp);
+        if (live) {
+            WMem<T, V> ws{w + rr * Cfg::NP * Nq, dw + rr * Cfg::NP * Nq, Nq, c0};
+            backward_body<Cfg, T, V>(xv, yv, ws, dz + rr * Cfg::D * Nq, 1.f, Nq, c0, dxa, dyp);
+        }
         group_reduce<Cfg::D2>(dyp, L.G);
         if (live) {
 #pragma unroll
@@ -377,14 +448,20 @@ __global__ void __launch_bounds__(256) tp_backward_kernel(int64_t R, int Nq, con
 // Convolution forward: one row group per receiver, all D output rows in registers, edges
 // of the receiver in CSR order (Alg. 2 receiver-stationary aggregation).
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T, int V>
+// RH > 0: the radial form (weights from the hidden activations h [E][RH] and the output
+// layer W2 [RH][NP][Nq], staged in dynamic shared memory; w unused)
+template <class Cfg, class T, int V, int RH = 0>
 __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E, int Nq,
                                                            const int32_t* __restrict__ rowptr,
                                                            const int32_t* __restrict__ sender,
                                                            const T* __restrict__ x, const T* __restrict__ y,
                                                            const T* __restrict__ w, float scale,
                                                            float* __restrict__ m, int64_t pad,
-                                                           unsigned* __restrict__ err) {
+                                                           unsigned* __restrict__ err,
+                                                           const float* __restrict__ hrad = nullptr,
+                                                           const float* __restrict__ W2 = nullptr) {
+    extern __shared__ __align__(16) float w2s[];
+    if constexpr (RH > 0) load_w2_shared(w2s, W2, RH * Cfg::NP * Nq);
     const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -414,14 +491,27 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
             float xv[Cfg::D1][V];
 #pragma unroll
             for (int i = 0; i < Cfg::D1; ++i) loadv<T, V>(x + (a * Cfg::D1 + i) * Nq + c0, xv[i]);
-            sfor<Cfg::NP>([&](auto pp) {
-                constexpr int p = decltype(pp)::value;
-                float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
-                build_A<Cfg, p>(yv, A);
-                float wv[V];
-                loadv<T, V>(w + (e * Cfg::NP + p) * Nq + c0, wv);
-                apply_path<Cfg, p, Cfg::D, V>(A, xv, wv, acc, Cfg::table.paths[p].zoff);
-            });
+            auto paths = [&](const auto& ws) {
+                sfor<Cfg::NP>([&](auto pp) {
+                    constexpr int p = decltype(pp)::value;
+                    float A[Off<Cfg>::a[p + 1] - Off<Cfg>::a[p]];
+                    build_A<Cfg, p>(yv, A);
+                    float wv[V];
+                    ws.get(p, wv);
+                    apply_path<Cfg, p, Cfg::D, V>(A, xv, wv, acc, Cfg::table.paths[p].zoff);
+                });
+            };
+            if constexpr (RH > 0) {
+                WRad<Cfg::NP, RH, V> ws;
+                ws.w2s = w2s;
+                ws.Nq = Nq;
+                ws.c0 = c0;
+#pragma unroll
+                for (int k = 0; k < RH; ++k) ws.h[k] = __ldg(hrad + e * RH + k);
+                paths(ws);
+            } else {
+                paths(WMem<T, V>{w + e * Cfg::NP * Nq, nullptr, Nq, c0});
+            }
         }
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i) {
@@ -438,12 +528,17 @@ __global__ void __launch_bounds__(256) conv_forward_kernel(int64_t N, int64_t E,
 // edges of a (csc_ptr / csc_edge / csc_recv), gathering dm of each receiver. dw and dy are
 // edge-local and written once per edge.
 // ------------------------------------------------------------------------------------------
-template <class Cfg, class T, int V>
+// RH > 0: the radial form; dw is then dh [E][RH] (the cotangent of the hidden activations,
+// sum over paths and channels of W2 dw) and w is unused
+template <class Cfg, class T, int V, int RH = 0>
 __global__ void __launch_bounds__(256) conv_backward_kernel(
     int64_t N, int64_t E, int Nq, const int32_t* __restrict__ csc_ptr, const int32_t* __restrict__ csc_edge,
     const int32_t* __restrict__ csc_recv, const T* __restrict__ x, const T* __restrict__ y,
     const T* __restrict__ w, const T* __restrict__ dm, float scale, float* __restrict__ dx,
-    float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err) {
+    float* __restrict__ dy, float* __restrict__ dw, int64_t pad, unsigned* __restrict__ err,
+    const float* __restrict__ hrad = nullptr, const float* __restrict__ W2 = nullptr) {
+    extern __shared__ __align__(16) float w2s[];
+    if constexpr (RH > 0) load_w2_shared(w2s, W2, RH * Cfg::NP * Nq);
     const Lanes L = lanes_for<V>(Nq);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -495,12 +590,32 @@ __global__ void __launch_bounds__(256) conv_backward_kernel(
             float dyp[Cfg::D2];
 #pragma unroll
             for (int t = 0; t < Cfg::D2; ++t) dyp[t] = 0.f;
-            if (ok) {
+            if constexpr (RH > 0) {
+                WRad<Cfg::NP, RH, V> ws;
+                ws.w2s = w2s;
+                ws.Nq = Nq;
+                ws.c0 = c0;
+#pragma unroll
+                for (int k = 0; k < RH; ++k) {
+                    ws.h[k] = ok ? __ldg(hrad + e * RH + k) : 0.f;
+                    ws.dh[k] = 0.f;
+                }
+                if (ok) {
+                    float yv[Cfg::D2];
+#pragma unroll
+                    for (int t = 0; t < Cfg::D2; ++t) yv[t] = IO<T>::load1(y + e * Cfg::D2 + t);
+                    backward_body<Cfg, T, V>(xv, yv, ws, dm + b * Cfg::D * Nq, scale, Nq, c0, dxa, dyp);
+                }
+                group_reduce<RH>(ws.dh, L.G);
+                if (ok && L.gl == 0)
+#pragma unroll
+                    for (int k = 0; k < RH; ++k) dw[e * RH + k] = ws.dh[k];
+            } else if (ok) {
                 float yv[Cfg::D2];
 #pragma unroll
                 for (int t = 0; t < Cfg::D2; ++t) yv[t] = IO<T>::load1(y + e * Cfg::D2 + t);
-                backward_body<Cfg, T, V>(xv, yv, w + e * Cfg::NP * Nq, dm + b * Cfg::D * Nq, scale,
-                                      dw + e * Cfg::NP * Nq, Nq, c0, dxa, dyp);
+                WMem<T, V> ws{w + e * Cfg::NP * Nq, dw + e * Cfg::NP * Nq, Nq, c0};
+                backward_body<Cfg, T, V>(xv, yv, ws, dm + b * Cfg::D * Nq, scale, Nq, c0, dxa, dyp);
             }
             group_reduce<Cfg::D2>(dyp, L.G);
             if (ok && L.gl == 0)
@@ -808,9 +923,20 @@ struct ConfigOps {
                                 const int32_t*, const int32_t*, const void*, const void*, const void*,
                                 const void*, const void*, const void*, const void*, float, void*, void*, void*,
                                 void*, int64_t, unsigned*, cudaStream_t);
+    // radial convolution (fp32, hidden width kRadialHidden): forward (..., x, y, h, W2, scale, m,
+    // pad, err, stream) and backward (..., x, y, h, W2, dm, scale, dx, dy, dh, pad, err, stream)
+    cudaError_t (*conv_fwd_rad)(int64_t, int64_t, int, const int32_t*, const int32_t*, const float*,
+                                const float*, const float*, const float*, float, float*, int64_t, unsigned*,
+                                cudaStream_t);
+    cudaError_t (*conv_bwd_rad)(int64_t, int64_t, int, const int32_t*, const int32_t*, const int32_t*,
+                                const float*, const float*, const float*, const float*, const float*, float,
+                                float*, float*, float*, int64_t, unsigned*, cudaStream_t);
 };
 
-int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units);
+// hidden width of the radial network that the radial convolution kernels are built for
+constexpr int kRadialHidden = 8;
+
+int grid_for(const void* kernel, int block, int64_t items_per_block_unit, int64_t units, int smem = 0);
 int sm_count();
 
 }  // namespace e3gb

@@ -99,7 +99,33 @@ def test_host_argument_checks_need_no_gpu(lib):
                                       ctypes.c_float(1.0), pad, None, None, None, 0, None) == e3.ERR_INVALID_ARG
     assert lib.e3gb_sh_forward(4, 3, None, None, 0, None) == e3.ERR_UNSUPPORTED
     assert lib.e3gb_graph_prepare(10, 20, None, None, None, None, None, None, 0, None) == e3.ERR_INVALID_ARG
-    assert lib.e3gb_graph_prepare_workspace_bytes(1000) >= 1001 * 4
+    # one 256-entry digit count per tile of 1024 edges, plus the scan's block sums
+    assert lib.e3gb_graph_prepare_workspace_bytes(1000, 5000) >= 256 * 5 * 4
+    assert lib.e3gb_graph_prepare_workspace_bytes(1000, 0) >= 0
+
+
+def test_radial_argument_checks_need_no_gpu(lib):
+    """The radial entry points reject bad network sizes, other dtypes and other hidden widths
+    on the host."""
+    f = ctypes.c_float
+    assert lib.e3gb_radial_hidden(0, None, None, 0, 8, f(4.0), None, None) == e3.ERR_INVALID_ARG
+    assert b"n_basis" in lib.e3gb_last_error()
+    assert lib.e3gb_radial_hidden(0, None, None, 8, 17, f(4.0), None, None) == e3.ERR_INVALID_ARG
+    assert lib.e3gb_radial_hidden(0, None, None, 8, 8, f(0.0), None, None) == e3.ERR_INVALID_ARG
+    assert lib.e3gb_radial_backward(5, None, None, 8, 8, f(4.0), None, None, 0, None) == e3.ERR_INVALID_ARG
+    t = e3.Table.create([(0, 1), (1, -1)], 16, 2, 2)
+    # bf16 and hidden widths other than the compiled one are not built
+    assert lib.e3gb_conv_forward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, 8, f(1.0), -1,
+                                        None, e3.BF16, None) == e3.ERR_UNSUPPORTED
+    assert lib.e3gb_conv_forward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, 4, f(1.0), -1,
+                                        None, e3.F32, None) == e3.ERR_UNSUPPORTED
+    assert lib.e3gb_conv_backward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, None, 16, None,
+                                         f(1.0), -1, None, None, None, e3.F32, None) == e3.ERR_UNSUPPORTED
+    assert lib.e3gb_conv_forward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, 8, f(1.0), 9,
+                                        None, e3.F32, None) == e3.ERR_INVALID_ARG
+    assert lib.e3gb_conv_forward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, 8, f(1.0), -1,
+                                        None, e3.F32, None) == e3.ERR_INVALID_ARG
+    assert b"NULL" in lib.e3gb_last_error()
 
 
 def test_table_coo_records_match_the_oracle_records():

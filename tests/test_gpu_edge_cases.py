@@ -60,6 +60,56 @@ def test_graph_prepare_heavy_sender_and_receiver():
     assert np.array_equal(cr.cpu().numpy(), recv[order])
 
 
+def test_graph_prepare_padding_node_of_huge_valency():
+    """Static-shape graphs send their unused edge slots from one padding node (e3j, Sec. 4
+    "Message passing convolution"): here 600k of 1M edges. The index must still be numpy's
+    stable argsort bit for bit, and its cost linear in the edges: well under 50 ms."""
+    N = 20_001
+    pad = N - 1
+    rng = np.random.default_rng(7)
+    n_real, n_pad_in, n_pad = 380_000, 20_000, 600_000
+    recv = np.concatenate([rng.integers(0, pad, n_real), rng.integers(0, pad, n_pad_in), np.full(n_pad, pad)])
+    send = np.concatenate([rng.integers(0, pad, n_real), np.full(n_pad_in, pad), np.full(n_pad, pad)])
+    srt = np.argsort(recv, kind="stable")
+    recv, send = recv[srt], send[srt]
+    rowptr = np.zeros(N + 1, np.int64)
+    np.cumsum(np.bincount(recv, minlength=N), out=rowptr[1:])
+    rp, sd = to_dev(rowptr.astype(np.int32)), to_dev(send.astype(np.int32))
+    cp, ce, cr = e3.graph_prepare(rp, sd, N)
+    ws = torch.empty(e3.graph_prepare_workspace_bytes(N, len(send)), dtype=torch.uint8, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    e3.graph_prepare(rp, sd, N, out=(cp, ce, cr), workspace=ws)
+    ev[1].record()
+    torch.cuda.synchronize()
+    assert e3.check_device_status() == 0
+    order = np.argsort(send, kind="stable")
+    ptr = np.zeros(N + 1, np.int64)
+    np.cumsum(np.bincount(send, minlength=N), out=ptr[1:])
+    assert np.array_equal(cp.cpu().numpy(), ptr)
+    assert np.array_equal(ce.cpu().numpy(), order)
+    assert np.array_equal(cr.cpu().numpy(), recv[order])
+    assert ev[0].elapsed_time(ev[1]) < 50.0
+
+
+def test_graph_prepare_edges_outside_rowptr_left_out():
+    """Edges before rowptr[0] or from rowptr[N] on belong to no receiver: they are left out
+    of the index (not flagged), and the entries past csc_ptr[N] are -1."""
+    g = random_graph(50, 600, (95, 3))
+    rp = g.rowptr.copy()
+    lo, hi = int(rp[1]), int(rp[-2])
+    rp[0], rp[-1] = lo, hi           # receiver 0 and receiver N-1 lose their edges
+    cp, ce, cr = e3.graph_prepare(to_dev(rp), to_dev(g.sender), g.n_nodes)
+    assert e3.check_device_status() == 0
+    keep = np.arange(lo, hi)
+    order = keep[np.argsort(g.sender[keep], kind="stable")]
+    n = len(keep)
+    assert int(cp[-1]) == n
+    assert np.array_equal(ce.cpu().numpy()[:n], order)
+    assert np.all(ce.cpu().numpy()[n:] == -1) and np.all(cr.cpu().numpy()[n:] == -1)
+    assert np.array_equal(cr.cpu().numpy()[:n], g.receiver()[order])
+
+
 def _run(t, g, x, w, dm, scale):
     rp, sd = to_dev(g.rowptr), to_dev(g.sender)
     y = e3.sh_forward(to_dev(g.vec.astype(np.float32)), t.sh_lmax)

@@ -2,10 +2,10 @@
 
 It serves callers that must not allocate device memory (a host that gave all free memory
 to its own pool, a plugin whose host owns every allocation, a latency-critical loop that
-cannot take cudaMalloc's device-wide synchronisation): the per-node counters live in a
+cannot take cudaMalloc's device-wide synchronisation): the sort's digit counts live in a
 static array inside the library instead of a caller workspace. Its result must equal that
 of e3gb_graph_prepare bit for bit, on consecutive calls (the array keeps the previous
-call's contents and has to be cleared by each call). This file sorts last so that a run
+call's contents, which no call may depend on). This file sorts last so that a run
 stopping at the first failure has already run every other test.
 """
 import ctypes
@@ -54,8 +54,37 @@ def test_static_prepare_equals_workspace_prepare(cuda):
         assert np.array_equal(got[1].cpu().numpy(), order)
 
 
-def test_static_prepare_rejects_too_many_nodes(cuda):
+def test_static_prepare_large_graph_with_longer_tiles(cuda):
+    """More than a million nodes and ~4.5 M edges: the library's array holds the counts of
+    ~4,000 tiles, so each tile covers 2,048 edges here (1,024 with a workspace). One edge
+    leaves the last node and one enters it. The result must still equal the workspace
+    entry point's bit for bit, and numpy's stable argsort."""
+    e3.load()
+    N, E = 1_200_000, 4_500_000
+    rng = np.random.default_rng(97)
+    recv = np.sort(rng.integers(0, N, E))
+    send = rng.integers(0, N, E)
+    send[E // 2] = N - 1
+    recv[-1] = N - 1
+    rowptr = np.zeros(N + 1, np.int64)
+    np.cumsum(np.bincount(recv, minlength=N), out=rowptr[1:])
+    rp = torch.from_numpy(rowptr.astype(np.int32)).cuda()
+    sd = torch.from_numpy(send.astype(np.int32)).cuda()
+    want = e3.graph_prepare(rp, sd, N)
+    for _ in range(2):
+        got = _static(rp, sd, N)
+        torch.cuda.synchronize()
+        assert e3.check_device_status() == 0
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    order = np.argsort(send, kind="stable")
+    assert np.array_equal(got[1].cpu().numpy(), order)
+    assert np.array_equal(got[2].cpu().numpy(), recv[order])
+    assert int(got[0][N - 1]) == E - int((send == N - 1).sum())
+
+
+def test_static_prepare_rejects_oversized_graphs(cuda):
     lib = e3.load()
-    st = lib.e3gb_graph_prepare_static(e3.STATIC_PREPARE_MAX_NODES + 1, 0, None, None, None, None, None, None)
+    st = lib.e3gb_graph_prepare_static(2 ** 31 - 1, 0, None, None, None, None, None, None)
     assert st == e3.ERR_INVALID_ARG
-    assert b"static scratch" in lib.e3gb_last_error()
+    assert b"e3gb_graph_prepare_static" in lib.e3gb_last_error()
