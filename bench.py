@@ -14,7 +14,7 @@ device -> host copies of all outputs inside the timed region (consecutive steps 
 copies and compute on three streams with two device buffer sets).
 
 Profiling options shrink single parts of the run (--atoms for the main step, --tp-rows,
---workload-atoms for the 8-channel workload, --dbwd-atoms, --workloads to pick timings).
+--workload-atoms for every conv workload's box, --dbwd-atoms, --workloads to pick timings).
 
 Throughput accounting follows "e3j ...", Sec. 3 Eq. (9): (bytes of inputs + outputs) /
 runtime, backward counting input primals, output cotangents and input cotangents.
@@ -55,6 +55,7 @@ def peaks():
 KERNEL_SOURCES = {
     "conv_fwd": ("conv_pipe.cuh", "kernels.cuh", "cg_table.hpp", "configs.def", "instances.cu"),
     "conv_bwd": ("conv_pipe.cuh", "kernels.cuh", "cg_table.hpp", "configs.def", "instances.cu"),
+    "tp_fwd": ("kernels.cuh", "cg_table.hpp", "configs.def", "instances.cu"),
 }
 
 
@@ -774,17 +775,20 @@ def run_ours(args):
         del wd, dmd, dx, dy, dw, xd, y, m
         torch.cuda.empty_cache()
         want = set(args.workloads.split(","))
+        na = args.workload_atoms   # a smaller box of every conv workload (profiling)
         jobs = [("tp1", lambda: time_tp_workload(W.WORKLOADS[1], dev, stream, 20, hbm_peak)),
-                ("conv4", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak)),
-                ("conv3", lambda: time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak)),
-                ("conv4bf16", lambda: time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak)),
+                ("conv4", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
+                                                     n_atoms=na)),
+                ("conv3", lambda: time_conv_workload(W.WORKLOADS[3], torch.float32, dev, stream, 5, hbm_peak,
+                                                     n_atoms=na)),
+                ("conv4bf16", lambda: time_conv_workload(W.WORKLOADS[4], torch.bfloat16, dev, stream, 5, hbm_peak,
+                                                         n_atoms=na)),
                 ("conv5", lambda: time_conv_workload(W.WORKLOADS[5], torch.float32, dev, stream, 5, hbm_peak,
-                                                     n_atoms=args.workload_atoms)),
+                                                     n_atoms=na)),
                 ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
-                                                   pad_frac=0.25)),
+                                                   pad_frac=0.25, n_atoms=na)),
                 ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak)),
-                ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak,
-                                                         n_atoms=args.atoms))]
+                ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na))]
         others = [f() for k, f in jobs if "all" in want or k in want]
         if "all" in want or "dbwd" in want:
             double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak, n_atoms=args.dbwd_atoms)
@@ -838,10 +842,11 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload kernel timings")
     ap.add_argument("--workloads", default="all",
-                    help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,dbwd (or all)")
+                    help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,radial4,dbwd "
+                         "(or all)")
     ap.add_argument("--dbwd-atoms", type=int, default=None, help="smaller double-backward case (profiling)")
     ap.add_argument("--workload-atoms", type=int, default=None,
-                    help="smaller box for the 8-channel workload's timing (profiling)")
+                    help="smaller box for every conv workload's timing (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

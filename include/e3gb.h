@@ -196,6 +196,26 @@ e3gb_status e3gb_conv_forward(const e3gb_table *t, int64_t n_nodes, int64_t n_ed
                               const void *y, const void *w, float scale, int64_t pad_node,
                               void *m, e3gb_dtype dtype, void *stream);
 
+/* e3gb_conv_forward for graphs with heavy receivers. A receiver-stationary forward gives each
+ * receiver to one warp, so one receiver with very many edges (a hub that is not the padding
+ * node) makes the whole launch wait for that warp (e3j, Sec. 4 "Message passing convolution":
+ * the receiver-degree imbalance that deterministic receiver-stationary kernels face). Here a
+ * receiver's CSR segment is cut into pieces of chunk positions: the first piece is summed by the
+ * usual kernels, every further piece by its own warp into a partial row set in the workspace,
+ * and the partials are added to m[b] in piece order. Deterministic (fixed order, no atomics);
+ * receivers with at most chunk positions get exactly e3gb_conv_forward's result, heavier ones
+ * a different (fixed) summation order. Arguments as e3gb_conv_forward, plus chunk >= 1 and a
+ * device workspace of at least e3gb_conv_forward_split_workspace_bytes bytes (16-byte
+ * aligned; contents on entry do not matter). E3GB_ERR_UNSUPPORTED for configurations with more
+ * than 32 output rows. */
+size_t e3gb_conv_forward_split_workspace_bytes(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                                               int32_t chunk);
+e3gb_status e3gb_conv_forward_split(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
+                                    const int32_t *rowptr, const int32_t *sender, const void *x,
+                                    const void *y, const void *w, float scale, int64_t pad_node,
+                                    int32_t chunk, void *m, void *workspace, size_t ws_bytes,
+                                    e3gb_dtype dtype, void *stream);
+
 /* Its VJP (Eq. 16) from dm [n_nodes,D,Nq]:
  *   dw[e,p] = scale * sum_m3 dm[b][blk p, m3] * (C_p(x[a], y[e]))[m3],
  *   dy[e]   = scale * sum over paths and channels of the x, w, dm couplings,

@@ -30,6 +30,7 @@ SYMBOLS = (
     "e3gb_graph_prepare", "e3gb_graph_prepare_static", "e3gb_conv_forward", "e3gb_conv_backward",
     "e3gb_conv_double_backward", "e3gb_coo_tp_forward", "e3gb_coo_tp_backward",
     "e3gb_radial_hidden", "e3gb_radial_backward", "e3gb_conv_forward_radial", "e3gb_conv_backward_radial",
+    "e3gb_conv_forward_split_workspace_bytes", "e3gb_conv_forward_split",
     "e3gb_check_device_status", "e3gb_last_error", "e3gb_version",
 )
 
@@ -89,6 +90,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "e3gb_conv_forward_radial": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, i32, f32, i64, vp, i32, vp]),
         "e3gb_conv_backward_radial": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp, f32, i64, vp, vp, vp,
                                             i32, vp]),
+        "e3gb_conv_forward_split_workspace_bytes": (szt, [vp, i64, i64, i32]),
+        "e3gb_conv_forward_split": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, f32, i64, i32, vp, vp, szt, i32, vp]),
         "e3gb_check_device_status": (i32, [vp, P32]),
         "e3gb_last_error": (ctypes.c_char_p, []),
         "e3gb_version": (ctypes.c_char_p, []),
@@ -380,6 +383,27 @@ def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stre
     _check(load().e3gb_conv_forward(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
                                     _ptr(y) if E else None, _ptr(w) if E else None, float(scale), int(pad_node), _ptr(m),
                                     _dtype(x, *((y, w) if E else ())), _stream(stream)))
+    return m
+
+
+def conv_forward_split(t: Table, rowptr, sender, x, y, w, scale: float, chunk: int = 1024, out=None, workspace=None,
+                       stream=None, pad_node: int = -1):
+    """conv_forward with receivers of more than `chunk` edges cut into pieces summed by separate
+    warps and added in piece order (deterministic); for graphs with heavy receivers."""
+    import torch
+    _contig(rowptr, sender, x, y, w)
+    N, E = x.shape[0], sender.shape[0]
+    _shape("rowptr", rowptr, N + 1)
+    _conv_operands(t, N, E, x, y, w)
+    m = out if out is not None else torch.empty((N, t.D, t.mul), dtype=torch.float32, device=x.device)
+    _shape("m", m, N, t.D, t.mul)
+    _f32_out(m)
+    nb = int(load().e3gb_conv_forward_split_workspace_bytes(t.handle, N, E, int(chunk)))
+    ws = workspace if workspace is not None else torch.empty(max(nb, 16), dtype=torch.uint8, device=x.device)
+    _check(load().e3gb_conv_forward_split(t.handle, N, E, _ptr(rowptr), _ptr(sender) if E else None, _ptr(x),
+                                          _ptr(y) if E else None, _ptr(w) if E else None, float(scale), int(pad_node),
+                                          int(chunk), _ptr(m), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _dtype(x, *((y, w) if E else ())), _stream(stream)))
     return m
 
 

@@ -414,8 +414,60 @@ e3gb_status e3gb_conv_forward(const e3gb_table* t, int64_t n_nodes, int64_t n_ed
     unsigned* err = error_word(&st);
     if (err == nullptr) return st;
     return cuda_status(t->ops->conv_fwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m, pad_node,
-                                               err, (cudaStream_t)stream),
+                                               err, INT64_MAX, (cudaStream_t)stream),
                        "conv_forward launch");
+}
+
+// the split forward's workspace: piece pointers, the scan's block sums, the partial rows
+static size_t split_workspace_bytes(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, int32_t chunk) {
+    const size_t ptr = size_t(n_nodes + 1 + 63) / 64 * 64;
+    const size_t sums = (scan_sums_count(n_nodes + 1) + 63) / 64 * 64;
+    const size_t pieces = size_t(n_edges / chunk + 1);
+    return (ptr + sums) * 4 + pieces * size_t(t->ops->D) * size_t(t->mul) * 4;
+}
+
+size_t e3gb_conv_forward_split_workspace_bytes(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, int32_t chunk) {
+    if (t == nullptr || t->ops == nullptr || n_nodes < 0 || n_edges < 0 || chunk < 1) return 0;
+    return split_workspace_bytes(t, n_nodes, n_edges, chunk);
+}
+
+e3gb_status e3gb_conv_forward_split(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* rowptr,
+                                    const int32_t* sender, const void* x, const void* y, const void* w, float scale,
+                                    int64_t pad_node, int32_t chunk, void* m, void* workspace, size_t ws_bytes,
+                                    e3gb_dtype dtype, void* stream) {
+    E3GB_TRY(check_table(t, dtype));
+    if (chunk < 1) return fail(E3GB_ERR_INVALID_ARG, "chunk must be >= 1");
+    if (t->ops->D > 32)
+        return fail(E3GB_ERR_UNSUPPORTED, "the split forward keeps at most 32 output rows per receiver (D = %d)",
+                    t->ops->D);
+    if (n_nodes < 0 || n_edges < 0) return fail(E3GB_ERR_INVALID_ARG, "negative size");
+    if (n_nodes >= INT32_MAX || n_edges >= INT32_MAX) return fail(E3GB_ERR_INVALID_ARG, "sizes must be < 2^31-1");
+    if (pad_node < -1 || pad_node >= n_nodes)
+        return fail(E3GB_ERR_INVALID_ARG, "pad_node %lld outside [-1, n_nodes)", (long long)pad_node);
+    if (n_nodes == 0) {
+        if (n_edges > 0) return fail(E3GB_ERR_BAD_GRAPH, "edges without nodes");
+        return ok();
+    }
+    const size_t need = split_workspace_bytes(t, n_nodes, n_edges, chunk);
+    if (ws_bytes < need) return fail(E3GB_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, need);
+    const size_t va = vec_align(dtype), ea = elt_bytes(dtype);
+    const bool edges = n_edges > 0;
+    E3GB_TRY(check_ptr(rowptr, "rowptr", 4, true));
+    E3GB_TRY(check_ptr(sender, "sender", 4, edges));
+    E3GB_TRY(check_ptr(x, "x", va, true));
+    E3GB_TRY(check_ptr(y, "y", ea, edges));
+    E3GB_TRY(check_ptr(w, "w", va, edges));
+    E3GB_TRY(check_ptr(m, "m", 16, true));
+    E3GB_TRY(check_ptr(workspace, "workspace", 16, true));
+    e3gb_status st = E3GB_OK;
+    unsigned* err = error_word(&st);
+    if (err == nullptr) return st;
+    E3GB_TRY(cuda_status(t->ops->conv_fwd[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m, pad_node,
+                                                 err, chunk, (cudaStream_t)stream),
+                         "conv_forward_split launch"));
+    return cuda_status(t->ops->conv_fwd_pieces[dtype](n_nodes, n_edges, t->mul, rowptr, sender, x, y, w, scale, m,
+                                                      pad_node, chunk, workspace, err, (cudaStream_t)stream),
+                       "conv_forward_split pieces launch");
 }
 
 e3gb_status e3gb_conv_backward(const e3gb_table* t, int64_t n_nodes, int64_t n_edges, const int32_t* csc_ptr,
@@ -499,6 +551,9 @@ static e3gb_status check_radial_conv(const e3gb_table* t, int64_t n_nodes, int64
     if (hidden != kRadialHidden)
         return fail(E3GB_ERR_UNSUPPORTED, "the radial convolution is built for hidden = %d (got %d)", kRadialHidden,
                     hidden);
+    if (t->ops->D > 32)
+        return fail(E3GB_ERR_UNSUPPORTED, "the radial convolution keeps at most 32 output rows per receiver (D = %d)",
+                    t->ops->D);
     if (t->ops->conv_fwd_rad == nullptr || int64_t(kRadialHidden) * t->ops->NP * t->mul * 4 > 232448)
         return fail(E3GB_ERR_UNSUPPORTED, "W2 of %d x %d x %d floats does not fit in shared memory", kRadialHidden,
                     t->ops->NP, t->mul);

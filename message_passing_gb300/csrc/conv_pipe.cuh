@@ -319,7 +319,7 @@ template <class Cfg, class T, int NSLOT, int WARPS, int RH = 0>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ sender,
                          const T* __restrict__ x, const T* __restrict__ y, const T* __restrict__ w, float scale,
-                         float* __restrict__ m, int64_t pad, unsigned* __restrict__ err,
+                         float* __restrict__ m, int64_t pad, unsigned* __restrict__ err, int64_t cap,
                          const float* __restrict__ hrad = nullptr, const float* __restrict__ W2 = nullptr) {
     using F = FwdPipe<Cfg, T, NSLOT, RH>;
     using PP = PipePlan<Cfg>;
@@ -350,7 +350,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
             const int64_t k0 = __ldg(rowptr + pn), k1 = __ldg(rowptr + pn + 1);
             const bool skip = pn == pad;
             pn += nw;
-            if (!skip && seg_ok(k0, k1, E)) { pe = k0; pend = k1; }
+            if (!skip && seg_ok(k0, k1, E)) { pe = k0; pend = k1 - k0 > cap ? k0 + cap : k1; }
         }
     };
     auto issue = [&](int64_t i) {   // issue the producer's current item into slot i % NSLOT
@@ -396,6 +396,7 @@ conv_forward_pipe_kernel(int64_t N, int64_t E, const int32_t* __restrict__ rowpt
             e0 = e1 = 0;
         }
         if (b == pad) e0 = e1 = 0;
+        if (e1 - e0 > cap) e1 = e0 + cap;   // the rest of a heavy receiver: conv_forward_pieces_kernel
         Q2 acc[Cfg::D];
 #pragma unroll
         for (int i = 0; i < Cfg::D; ++i) acc[i] = q2_zero();
@@ -762,7 +763,8 @@ struct PipeShape {
     static constexpr int by_smem = (kSmemLimit - W2B) / WARP_BYTES;
     static constexpr int WARPS = by_smem < 8 ? by_smem : 8;
     static constexpr int SMEM = W2B + WARPS * WARP_BYTES;
-    static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4;
+    // the forward keeps every output row of its receiver in registers: at most 32 of them
+    static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4 && (BWD || Cfg::D <= 32);
 };
 
 }  // namespace e3gb

@@ -485,7 +485,9 @@ struct DdPipeShape {
     static constexpr int by_smem = kSmemLimit / WARP_BYTES;
     static constexpr int WARPS = by_smem < 8 ? by_smem : 8;
     static constexpr int SMEM = WARPS * WARP_BYTES;
-    static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4 && 2 * (Cfg::D2 * sizeof(T) + 15) / 16 <= 32;
+    // the receiver pass keeps every output row of its receiver in registers: at most 32
+    static constexpr bool usable = (Cfg::D2 * sizeof(T)) % 16 == 0 && WARPS >= 4 &&
+                                   2 * (Cfg::D2 * sizeof(T) + 15) / 16 <= 32 && (SENDER || Cfg::D <= 32);
 };
 
 }  // namespace e3gb

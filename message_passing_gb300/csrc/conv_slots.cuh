@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(256) conv_forward_slots_kernel(int64_t N, int6
                                                                  const T* __restrict__ x, const T* __restrict__ y,
                                                                  const T* __restrict__ w, float scale,
                                                                  float* __restrict__ m, int64_t pad,
-                                                                 unsigned* __restrict__ err) {
+                                                                 unsigned* __restrict__ err, int64_t cap) {
     using SL = Slots<NQ>;
     constexpr int R = pow2_at_least(Cfg::D > SL::SPR ? Cfg::D : SL::SPR);
     const int lane = threadIdx.x & 31;
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(256) conv_forward_slots_kernel(int64_t N, int6
                 if (lane % (SL::G * SL::SPR) == 0) atomicOr(err, kErrRowptr);
                 e0 = e1 = 0;
             }
+            if (e1 - e0 > cap) e1 = e0 + cap;   // the rest of a heavy receiver: the pieces kernel
         }
         Q2 acc[R];
 #pragma unroll

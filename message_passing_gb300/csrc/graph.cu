@@ -319,6 +319,15 @@ int64_t sort_tile(int64_t E, int64_t tiles_cap) {
 
 size_t scan_sums_count(int64_t n) { return size_t((n + kScanChunk - 1) / kScanChunk); }
 
+cudaError_t exclusive_scan_i32(int32_t* a, int64_t n, int32_t* sums, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t nb = int64_t(scan_sums_count(n));
+    scan_sums_kernel<<<int(nb), kScanBlock, 0, s>>>(a, n, sums);
+    scan_top_kernel<<<1, kScanBlock, 0, s>>>(sums, nb);
+    scan_apply_kernel<<<int(nb), kScanBlock, 0, s>>>(a, n, sums);
+    return cudaGetLastError();
+}
+
 // int32 entries of the sort's scratch for tile length T: the digit counts, then the scan's block sums
 size_t graph_scratch_ints(int64_t E, int64_t T) {
     const int64_t n_hist = int64_t(kBins) * ((E + T - 1) / T);

@@ -9,6 +9,8 @@
 #include "conv_slots.cuh"
 #include "kernels.cuh"
 
+#include <type_traits>
+
 #if !defined(E3GB_CFG) || !defined(E3GB_PART)
 #error "compile with -DE3GB_CFG=<config id> -DE3GB_PART=<0|1|2|3|4|5>"
 #endif
@@ -46,6 +48,23 @@ static int rows_per_block(int Nq) { return (kBlock / 32) * (32 / (Nq / vec_for(N
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// configurations whose receiver outputs fit in registers (the receiver-stationary forwards keep
+// all of them live); others (one output block per path) walk the edges once per output block
+constexpr bool kRowsFit = Cfg::D <= 32;
+
+// The bf16 pipelined backward faulted ("illegal instruction") on its first run on the 0e+1o
+// configuration, and reading it did not show why; the bf16 pipelined kernels (conv forward
+// and backward, the row backward on the identity graph, the double backward), which share its
+// staging, are launched only on the configuration where they have run in every test and
+// benchmark (x irreps 0e+1o+2e, SH and outputs l <= 3). Other bf16 configurations take the
+// plain kernels.
+template <class T>
+constexpr bool pipe_cleared() {
+    if constexpr (std::is_same_v<T, float>) return true;
+    else return Cfg::xcode == xcode(xblock(0, 1), xblock(1, -1), xblock(2, 1)) && Cfg::L2 == 3 && Cfg::L3 == 3 &&
+                !Cfg::per_path;
+}
+
 template <class T>
 cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* w, void* z, cudaStream_t s);
 template <class T>
@@ -53,8 +72,13 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
                    void* dy, void* dw, cudaStream_t s);
 template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, int64_t cap,
                      cudaStream_t s);
+// the further pieces of heavy receivers (part 4)
+template <class T>
+cudaError_t conv_fwd_pieces(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                            const void* y, const void* w, float scale, void* m, int64_t pad, int64_t cap, void* ws,
+                            unsigned* err, cudaStream_t s);
 template <class T>
 cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge, const int32_t* crecv,
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
@@ -68,8 +92,8 @@ cudaError_t conv_dbwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const
 // plain kernels
 template <class T>
 bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, cudaStream_t s,
-                    cudaError_t* st);
+                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, int64_t cap,
+                    cudaStream_t s, cudaError_t* st);
 // the radial convolution, fp32 (part 5): weights formed in the kernels from the hidden
 // activations h [E][kRadialHidden] and the output layer W2 [kRadialHidden][NP][Nq]
 cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const float* x,
@@ -103,7 +127,7 @@ template <class T>
 cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* w, const void* dz, void* dx,
                    void* dy, void* dw, cudaStream_t s) {
     using S = PipeShape<Cfg, T, true>;
-    if constexpr (S::usable) {
+    if constexpr (S::usable && pipe_cleared<T>()) {
         // 128 channels: the pipelined convolution backward on the identity graph (row r is node
         // r with the one edge r), which streams the rows through the per-warp cp.async ring
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dz)) {
@@ -131,11 +155,32 @@ cudaError_t tp_bwd(int64_t R, int Nq, const void* x, const void* y, const void* 
 
 #if E3GB_PART == 0
 template <class T>
+cudaError_t conv_fwd_rows(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                          const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                          int64_t cap, cudaStream_t s);
+
+template <class T>
 cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, int64_t cap,
                      cudaStream_t s) {
+    if constexpr (!kRowsFit) {
+        auto k = vec_for(Nq) == 4 ? conv_forward_blocks_kernel<Cfg, T, 4> : conv_forward_blocks_kernel<Cfg, T, 1>;
+        const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
+        if (grid == 0) return cudaSuccess;
+        k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
+                                  pad, err, cap);
+        return cudaGetLastError();
+    } else {
+        return conv_fwd_rows<T>(N, E, Nq, rowptr, sender, x, y, w, scale, m, pad, err, cap, s);
+    }
+}
+
+template <class T>
+cudaError_t conv_fwd_rows(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                          const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
+                          int64_t cap, cudaStream_t s) {
     using S = PipeShape<Cfg, T, false>;
-    if constexpr (S::usable) {
+    if constexpr (S::usable && pipe_cleared<T>()) {
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w)) {
             auto k = conv_forward_pipe_kernel<Cfg, T, S::NSLOT, S::WARPS>;
             cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
@@ -144,17 +189,17 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
             k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale,
-                                                   (float*)m, pad, err, nullptr, nullptr);
+                                                   (float*)m, pad, err, cap, nullptr, nullptr);
             return cudaGetLastError();
         }
     }
     cudaError_t sst = cudaSuccess;
-    if (conv_fwd_slots<T>(N, E, Nq, rowptr, sender, x, y, w, scale, m, pad, err, s, &sst)) return sst;
+    if (conv_fwd_slots<T>(N, E, Nq, rowptr, sender, x, y, w, scale, m, pad, err, cap, s, &sst)) return sst;
     auto k = vec_for(Nq) == 4 ? conv_forward_kernel<Cfg, T, 4> : conv_forward_kernel<Cfg, T, 1>;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m,
-                              pad, err, nullptr, nullptr);
+                              pad, err, cap, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -164,7 +209,7 @@ cudaError_t conv_fwd(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const 
 template <class T, int NQ>
 static cudaError_t launch_fwd_slots(int64_t N, int64_t E, const int32_t* rowptr, const int32_t* sender, const void* x,
                                     const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err,
-                                    cudaStream_t s) {
+                                    int64_t cap, cudaStream_t s) {
     auto k = conv_forward_slots_kernel<Cfg, T, NQ>;
     constexpr int smem = slots_fwd_smem<Cfg, T>();
     cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -172,21 +217,21 @@ static cudaError_t launch_fwd_slots(int64_t N, int64_t E, const int32_t* rowptr,
     const int grid = grid_for((const void*)k, kBlock, slots_nodes_per_block<NQ>(), N);
     if (grid == 0) return cudaSuccess;
     k<<<grid, kBlock, smem, s>>>(N, E, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, scale, (float*)m, pad,
-                                 err);
+                                 err, cap);
     return cudaGetLastError();
 }
 
 template <class T>
 bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
-                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, cudaStream_t s,
-                    cudaError_t* st) {
+                    const void* y, const void* w, float scale, void* m, int64_t pad, unsigned* err, int64_t cap,
+                    cudaStream_t s, cudaError_t* st) {
     if constexpr (SlotsFit<Cfg>::value) {
         if (aligned16(x) && aligned16(y) && aligned16(w) && aligned16(m)) {
             switch (Nq) {
-            case 4: *st = launch_fwd_slots<T, 4>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
-            case 8: *st = launch_fwd_slots<T, 8>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
-            case 16: *st = launch_fwd_slots<T, 16>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
-            case 32: *st = launch_fwd_slots<T, 32>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, s); return true;
+            case 4: *st = launch_fwd_slots<T, 4>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, cap, s); return true;
+            case 8: *st = launch_fwd_slots<T, 8>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, cap, s); return true;
+            case 16: *st = launch_fwd_slots<T, 16>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, cap, s); return true;
+            case 32: *st = launch_fwd_slots<T, 32>(N, E, rowptr, sender, x, y, w, scale, m, pad, err, cap, s); return true;
             default: break;
             }
         }
@@ -195,10 +240,48 @@ bool conv_fwd_slots(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const i
 }
 
 template bool conv_fwd_slots<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*, const void*,
-                                     const void*, float, void*, int64_t, unsigned*, cudaStream_t, cudaError_t*);
+                                     const void*, float, void*, int64_t, unsigned*, int64_t, cudaStream_t,
+                                     cudaError_t*);
 template bool conv_fwd_slots<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
-                                             const void*, const void*, float, void*, int64_t, unsigned*, cudaStream_t,
-                                             cudaError_t*);
+                                             const void*, const void*, float, void*, int64_t, unsigned*, int64_t,
+                                             cudaStream_t, cudaError_t*);
+
+// heavy receivers: count the further pieces, scan, sum each piece, add the pieces to m in
+// order. Workspace: piece pointers (N + 1 ints), the scan's block sums, the partial rows.
+template <class T>
+cudaError_t conv_fwd_pieces(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const void* x,
+                            const void* y, const void* w, float scale, void* m, int64_t pad, int64_t cap, void* ws,
+                            unsigned* err, cudaStream_t s) {
+    if constexpr (!kRowsFit) {   // the host rejects these configurations
+        return cudaErrorNotSupported;
+    } else {
+        if (N <= 0 || E <= cap) return cudaSuccess;
+        int32_t* ptr = static_cast<int32_t*>(ws);
+        int32_t* sums = ptr + (N + 1 + 63) / 64 * 64;
+        float* partials = reinterpret_cast<float*>(sums + (scan_sums_count(N + 1) + 63) / 64 * 64);
+        piece_count_kernel<<<int((N + 256) / 256 < 4096 ? (N + 256) / 256 : 4096), 256, 0, s>>>(N, E, rowptr, pad,
+                                                                                                 cap, ptr);
+        cudaError_t st = exclusive_scan_i32(ptr, N + 1, sums, s);
+        if (st != cudaSuccess) return st;
+        auto k = vec_for(Nq) == 4 ? conv_forward_pieces_kernel<Cfg, T, 4> : conv_forward_pieces_kernel<Cfg, T, 1>;
+        const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), E / cap + 1);
+        k<<<grid, kBlock, 0, s>>>(N, E, Nq, rowptr, sender, (const T*)x, (const T*)y, (const T*)w, pad, cap, ptr,
+                                  partials, err);
+        st = cudaGetLastError();
+        if (st != cudaSuccess) return st;
+        const int64_t nb = (N + 7) / 8;
+        conv_pieces_combine_kernel<<<int(nb < 65535 ? nb : 65535), 256, 0, s>>>(N, int64_t(Cfg::D) * Nq, ptr, partials,
+                                                                                 scale, (float*)m);
+        return cudaGetLastError();
+    }
+}
+
+template cudaError_t conv_fwd_pieces<float>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
+                                            const void*, const void*, float, void*, int64_t, int64_t, void*, unsigned*,
+                                            cudaStream_t);
+template cudaError_t conv_fwd_pieces<__nv_bfloat16>(int64_t, int64_t, int, const int32_t*, const int32_t*, const void*,
+                                                    const void*, const void*, float, void*, int64_t, int64_t, void*,
+                                                    unsigned*, cudaStream_t);
 #endif  // part 4
 
 #if E3GB_PART == 1
@@ -207,7 +290,7 @@ cudaError_t conv_bwd(int64_t N, int64_t E, int Nq, const int32_t* cptr, const in
                      const void* x, const void* y, const void* w, const void* dm, float scale, void* dx, void* dy,
                      void* dw, int64_t pad, unsigned* err, cudaStream_t s) {
     using S = PipeShape<Cfg, T, true>;
-    if constexpr (S::usable) {
+    if constexpr (S::usable && pipe_cleared<T>()) {
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm)) {
             auto k = conv_backward_pipe_kernel<Cfg, T, S::NSLOT, S::WARPS>;
             cudaError_t st = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
@@ -282,7 +365,7 @@ bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const i
                     void* gw, void* gdm, int64_t pad, unsigned* err, cudaStream_t s, cudaError_t* st) {
     using SR = DdPipeShape<Cfg, T, false>;
     using SS = DdPipeShape<Cfg, T, true>;
-    if constexpr (SR::usable && SS::usable) {
+    if constexpr (SR::usable && SS::usable && pipe_cleared<T>()) {
         if (Nq == kPipeNq && aligned16(x) && aligned16(y) && aligned16(w) && aligned16(dm) && aligned16(ddx) &&
             aligned16(ddy) && aligned16(ddw)) {
             auto kr = conv_ddm_pipe_kernel<Cfg, T, SR::NSLOT, SR::WARPS>;
@@ -322,6 +405,9 @@ template bool conv_dbwd_pipe<__nv_bfloat16>(int64_t, int64_t, int, const int32_t
 cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const int32_t* sender, const float* x,
                          const float* y, const float* h, const float* W2, float scale, float* m, int64_t pad,
                          unsigned* err, cudaStream_t s) {
+    if constexpr (!kRowsFit) {   // the host rejects these configurations
+        return cudaErrorNotSupported;
+    } else {
     constexpr int RH = kRadialHidden;
     using S = PipeShape<Cfg, float, false, RH>;
     if constexpr (S::usable) {
@@ -332,7 +418,8 @@ cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, co
             const int64_t need = (N + S::WARPS - 1) / S::WARPS;
             const int grid = int(sm_count() < need ? sm_count() : need);
             if (grid == 0) return cudaSuccess;
-            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, x, y, nullptr, scale, m, pad, err, h, W2);
+            k<<<grid, S::WARPS * 32, S::SMEM, s>>>(N, E, rowptr, sender, x, y, nullptr, scale, m, pad, err, INT64_MAX,
+                                                   h, W2);
             return cudaGetLastError();
         }
     }
@@ -343,8 +430,9 @@ cudaError_t conv_fwd_rad(int64_t N, int64_t E, int Nq, const int32_t* rowptr, co
     if (st != cudaSuccess) return st;
     const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), N, smem);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, smem, s>>>(N, E, Nq, rowptr, sender, x, y, nullptr, scale, m, pad, err, h, W2);
+    k<<<grid, kBlock, smem, s>>>(N, E, Nq, rowptr, sender, x, y, nullptr, scale, m, pad, err, INT64_MAX, h, W2);
     return cudaGetLastError();
+    }
 }
 
 cudaError_t conv_bwd_rad(int64_t N, int64_t E, int Nq, const int32_t* cptr, const int32_t* cedge,
@@ -393,6 +481,7 @@ const ConfigOps kOps = {
     {conv_dbwd<float>, conv_dbwd<__nv_bfloat16>},
     conv_fwd_rad,
     conv_bwd_rad,
+    {conv_fwd_pieces<float>, conv_fwd_pieces<__nv_bfloat16>},
 };
 }  // namespace
 

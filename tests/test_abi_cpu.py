@@ -23,6 +23,7 @@ CONFIGS = [
     ([(0, 1)], 4, 0, 0, False),
     ([(1, -1)], 4, 1, 2, True),
     ([(0, 1), (1, -1)], 16, 2, 2, True),
+    ([(0, 1), (1, -1), (2, 1)], 128, 3, 3, True),
 ]
 
 
@@ -126,6 +127,26 @@ def test_radial_argument_checks_need_no_gpu(lib):
     assert lib.e3gb_conv_forward_radial(t.handle.value, 4, 5, None, None, None, None, None, None, 8, f(1.0), -1,
                                         None, e3.F32, None) == e3.ERR_INVALID_ARG
     assert b"NULL" in lib.e3gb_last_error()
+
+
+def test_split_forward_argument_checks_need_no_gpu(lib):
+    f = ctypes.c_float
+    t = e3.Table.create([(0, 1), (1, -1)], 16, 2, 2)
+    # workspace: piece pointers and scan sums for N + 1 entries, E / chunk + 1 partial row sets
+    nb = lib.e3gb_conv_forward_split_workspace_bytes(t.handle.value, 100, 5000, 64)
+    assert nb >= (5000 // 64 + 1) * t.D * t.mul * 4
+    assert lib.e3gb_conv_forward_split_workspace_bytes(t.handle.value, 100, 5000, 0) == 0
+    args = lambda chunk, ws: (t.handle.value, 4, 5, None, None, None, None, None, f(1.0), -1, chunk, None, None, ws,
+                              e3.F32, None)
+    assert lib.e3gb_conv_forward_split(*args(0, 1 << 20)) == e3.ERR_INVALID_ARG
+    assert b"chunk" in lib.e3gb_last_error()
+    assert lib.e3gb_conv_forward_split(*args(8, 16)) == e3.ERR_INVALID_ARG
+    assert b"workspace" in lib.e3gb_last_error()
+    # one output block per path on 0e+1o+2e: 106 rows per receiver, not built for the split form
+    tp = e3.Table.create([(0, 1), (1, -1), (2, 1)], 128, 3, 3, per_path=True)
+    assert tp.D == 106
+    assert lib.e3gb_conv_forward_split(tp.handle.value, 4, 5, None, None, None, None, None, f(1.0), -1, 8, None, None,
+                                       1 << 30, e3.F32, None) == e3.ERR_UNSUPPORTED
 
 
 def test_table_coo_records_match_the_oracle_records():

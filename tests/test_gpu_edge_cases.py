@@ -178,6 +178,14 @@ def test_determinism_bitwise():
         again = _run(t, g, x, ww, dm, 0.02)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+    # bf16 storage at 128 channels (the plain forward on this configuration)
+    xb, wb, dmb = (torch.from_numpy(a).to(torch.bfloat16) for a in (x, ww, dm))
+    yb = e3.sh_forward(to_dev(g.vec.astype(np.float32)), 3, dtype=torch.bfloat16)
+    rp, sd = to_dev(g.rowptr), to_dev(g.sender)
+    xb, wb = xb.cuda(), wb.cuda()
+    m0 = e3.conv_forward(t, rp, sd, xb, yb, wb, 0.02)
+    for _ in range(9):
+        assert torch.equal(m0, e3.conv_forward(t, rp, sd, xb, yb, wb, 0.02))
     # 8 channels: the edge-slot forward, whose slot sums are added in a fixed order
     w5 = W.WORKLOADS[5]
     t5 = e3.Table.create(w5.blocks, w5.mul, 3, 3)

@@ -108,9 +108,10 @@ def test_tp_channel_counts(mul):
 # ------------------------------------------------------------------------------------------
 # convolution
 # ------------------------------------------------------------------------------------------
-def _conv_gpu(t, rowptr, sender, vec32, x, ww, dm, scale, dtype=torch.float32):
+def _conv_gpu(t, rowptr, sender, vec32, x, ww, dm, scale, dtype=torch.float32, y=None):
     rp, sd = to_dev(rowptr), to_dev(sender)
-    y = e3.sh_forward(to_dev(vec32), t.sh_lmax, dtype=dtype)
+    if y is None:
+        y = e3.sh_forward(to_dev(vec32), t.sh_lmax, dtype=dtype)
     xd = x if torch.is_tensor(x) else to_dev(x, dtype)
     wd = ww if torch.is_tensor(ww) else to_dev(ww, dtype)
     dmd = dm if torch.is_tensor(dm) else to_dev(dm, dtype)
@@ -121,8 +122,9 @@ def _conv_gpu(t, rowptr, sender, vec32, x, ww, dm, scale, dtype=torch.float32):
     return m, dx, dy, dw
 
 
-def _conv_check(w, g, tol=TOL_F32, k_nodes=None, k_edges=None, dtype=torch.float32, device_w=False):
-    t, ot = _tables(w)
+def _conv_check(w, g, tol=TOL_F32, k_nodes=None, k_edges=None, dtype=torch.float32, device_w=False,
+                per_path=False):
+    t, ot = _tables(w, per_path)
     N, E = g.n_nodes, g.n_edges
     scale = N / max(E, 1)
     x, _ = W.make_conv(w, g, ot.n_paths, edge_ids=np.zeros(0, np.int64))
@@ -134,14 +136,20 @@ def _conv_check(w, g, tol=TOL_F32, k_nodes=None, k_edges=None, dtype=torch.float
         wd, dmd = to_dev(wn, dtype), to_dev(W.make_grad(w, N, ot.D), dtype)
     xd = to_dev(x, dtype)
     vec32 = g.vec.astype(np.float32)
-    m, dx, dy, dw = _conv_gpu(t, g.rowptr, g.sender, vec32, xd, wd, dmd, scale, dtype)
+    yo = oracle.sh(vec32.astype(np.float64), w.sh_lmax)
+    yd = None
+    if dtype == torch.bfloat16:
+        # both sides take the same stored bf16 harmonics: rounding the GPU's and the oracle's
+        # harmonics to bf16 separately can differ by one bf16 step where a value sits at a
+        # rounding midpoint (the SH kernel is checked on its own)
+        yb = torch.from_numpy(yo.astype(np.float32)).to(torch.bfloat16)
+        yo = to_np(yb)
+        yd = yb.cuda()
+    m, dx, dy, dw = _conv_gpu(t, g.rowptr, g.sender, vec32, xd, wd, dmd, scale, dtype, y=yd)
     torch.cuda.synchronize()
     # the oracle reads exactly the stored (possibly bf16-rounded) inputs, widened to f64
     xo = to_np(xd)
     dmo = to_np(dmd)
-    yo = oracle.sh(vec32.astype(np.float64), w.sh_lmax)
-    if dtype == torch.bfloat16:
-        yo = to_np(torch.from_numpy(yo.astype(np.float32)).to(torch.bfloat16))
     wfetch = lambda ids: to_np(wd[torch.from_numpy(np.asarray(ids, np.int64)).cuda()])
     nodes = np.arange(N) if k_nodes is None else sample_ids(N, k_nodes, 11)
     edges = np.arange(E) if k_edges is None else sample_ids(E, k_edges, 12)
@@ -195,9 +203,26 @@ def test_conv_mace_like_full_size_bf16():
     torch.cuda.empty_cache()
 
 
-def test_conv_bf16_reduced():
+@pytest.mark.parametrize("wid,atoms", [(4, 300), (3, 400)])
+def test_conv_bf16_reduced(wid, atoms):
+    """bf16 storage at 128 channels: the pipelined kernels (0e+1o+2e) and the plain ones
+    (0e+1o, where the bf16 pipelined kernels are not launched)."""
+    w = W.WORKLOADS[wid]
+    _conv_check(w, W.make_graph(w, n_atoms=atoms), tol=TOL_BF16, dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_conv_per_path_outputs_128_channels(dt):
+    """One output block per path (e3j's default layout, App. E.1) on the 64k workload's irreps:
+    106 output rows per node, so the forward walks each receiver's edges once per block."""
     w = W.WORKLOADS[4]
-    _conv_check(w, W.make_graph(w, n_atoms=300), tol=TOL_BF16, dtype=torch.bfloat16)
+    _conv_check(w, W.make_graph(w, n_atoms=250), tol=TOL_BF16 if dt == torch.bfloat16 else TOL_F32, dtype=dt,
+                per_path=True)
+
+
+def test_tp_per_path_outputs_128_channels():
+    w = W.Workload(94, "per-path", "tp", "128x0e+128x1o+128x2e", 3, 3, rows=777)
+    _tp_check(w, None, per_path=True)
 
 
 def test_conv_high_l_low_channel_reduced():
