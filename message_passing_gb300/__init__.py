@@ -590,3 +590,42 @@ def check_device_status(stream=None) -> int:
     if st != OK:
         raise E3GBError(st, load().e3gb_last_error().decode())
     return flags.value
+
+
+def shard_graphs(graph_ptr, rowptr, sender, world: int, rank: int) -> tuple[int, int, int, int]:
+    """Data-parallel split of a batch of independent graphs (molecules) stored as one
+    receiver-sorted CSR: graph g owns nodes [graph_ptr[g], graph_ptr[g+1]) and every edge into
+    them, and each of its edges must come from one of its own nodes. Returns (n0, n1, e0, e1):
+    rank's contiguous run of whole graphs, cut at the graph boundaries nearest to r * E / world
+    so that the ranks' edge counts differ by at most about one graph's edges. The rank's own
+    CSR is rowptr[n0:n1+1] - e0 with senders sender[e0:e1] - n0; no edge crosses ranks, so
+    the ranks exchange nothing on the data path (host logic, numpy; raises ValueError if an
+    edge leaves its graph)."""
+    import numpy as np
+
+    gp = np.asarray(graph_ptr, dtype=np.int64)
+    rp = np.asarray(rowptr, dtype=np.int64)
+    sd = np.asarray(sender, dtype=np.int64)
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside world {world}")
+    N, E = rp.shape[0] - 1, int(rp[-1]) if rp.shape[0] else 0
+    if gp.ndim != 1 or gp.shape[0] < 1 or gp[0] != 0 or gp[-1] != N or np.any(np.diff(gp) < 0):
+        raise ValueError("graph_ptr must rise from 0 to the node count")
+    if rp[0] != 0 or np.any(np.diff(rp) < 0) or sd.shape[0] != E:
+        raise ValueError("rowptr / sender do not form a CSR")
+    # the graph of each edge's receiver and of its sender must agree
+    recv = np.repeat(np.arange(N, dtype=np.int64), np.diff(rp))
+    g_of = lambda v: np.searchsorted(gp, v, side="right") - 1
+    if E and (np.any(sd < 0) or np.any(sd >= N) or np.any(g_of(recv) != g_of(sd))):
+        raise ValueError("an edge joins two graphs: the batch cannot be split without a halo")
+    eb = rp[gp]   # edge offset at each graph boundary (non-decreasing)
+    cut = [0]
+    for r in range(1, world):
+        t = r * E / world
+        b = int(np.searchsorted(eb, t))
+        if b > 0 and (b >= eb.shape[0] or t - eb[b - 1] <= eb[b] - t):
+            b -= 1
+        cut.append(max(b, cut[-1]))
+    cut.append(gp.shape[0] - 1)
+    n0, n1 = int(gp[cut[rank]]), int(gp[cut[rank + 1]])
+    return n0, n1, int(rp[n0]), int(rp[n1])
