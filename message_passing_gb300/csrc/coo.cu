@@ -7,7 +7,8 @@
 // Two forms:
 // - sorted plan (up to 8,192 records; index widths 11/10/11 bits): each block sorts the records
 //   into its shared memory by output row (forward) or path (backward), stably, so the records
-//   of one index form a run whose sum (z row; w and dw rows) lives in registers;
+//   of one index form a run whose sum (z row; w and dw rows, and the dx row of consecutive
+//   records of one x row) lives in registers;
 // - the general form: the whole warp reads the records in the given order (broadcast loads
 //   through L1) and each row group accumulates its outputs in its own shared-memory rows.
 // In both, records may come in any order and repeat, every output row is written, each lane
@@ -312,25 +313,42 @@ __global__ void __launch_bounds__(256, 1) coo_plan_backward_kernel(int64_t R, in
             loadv<T, V>(w + (rr * P + p) * Nq + c0, wv);
 #pragma unroll
             for (int c = 0; c < V; ++c) dwp[c] = 0.f;
+            // consecutive records of one x row (the usual order inside a path) load it once and
+            // add their dx share in registers, flushed to the shared dx row when the row changes
+            int cur_i1 = -1;
+            float xv[V], dxr[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) xv[c] = dxr[c] = 0.f;
 #pragma unroll 4
             for (int k = k0; k < k1; ++k) {
                 const CooRec q = srec[k];
                 const int i0 = q.idx & 0x7ff, i2 = (q.idx >> 11) & 0x3ff, i1 = q.idx >> 21;
-                float gv[V], xv[V];
+                if (i1 != cur_i1) {   // warp-uniform: every lane reads the same record
+                    if (cur_i1 >= 0)
+#pragma unroll
+                        for (int c = 0; c < V; ++c) gx[cur_i1 * Nq + c0 + c] += dxr[c];
+                    loadv<T, V>(xr + i1 * Nq, xv);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) dxr[c] = 0.f;
+                    cur_i1 = i1;
+                }
+                float gv[V];
                 loadv<T, V>(dzr + i0 * Nq, gv);
-                loadv<T, V>(xr + i1 * Nq, xv);
                 const float yv = IO<T>::load1(yr + i2);
                 float s = 0.f;
 #pragma unroll
                 for (int c = 0; c < V; ++c) {
                     const float g = q.c * gv[c];
                     const float gy = g * yv;
-                    gx[i1 * Nq + c0 + c] = fmaf(gy, wv[c], gx[i1 * Nq + c0 + c]);   // dx[i1]
-                    dwp[c] = fmaf(gy, xv[c], dwp[c]);                               // dw[path]
-                    s = fmaf(g * wv[c], xv[c], s);                                  // dy[i2] partial
+                    dxr[c] = fmaf(gy, wv[c], dxr[c]);     // dx[i1]
+                    dwp[c] = fmaf(gy, xv[c], dwp[c]);     // dw[path]
+                    s = fmaf(g * wv[c], xv[c], s);        // dy[i2] partial
                 }
                 dyl[i2 * 32 + lane] += s;
             }
+            if (cur_i1 >= 0)
+#pragma unroll
+                for (int c = 0; c < V; ++c) gx[cur_i1 * Nq + c0 + c] += dxr[c];
             if (live) storev<V>(dw + (rr * P + p) * Nq + c0, dwp);   // every path row, zero without records
         }
         __syncwarp();
