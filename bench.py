@@ -404,6 +404,66 @@ def radial_flops(E, nnz, P, D, Nq, H):
     return conv + wts, 2.0 * conv + 2.0 * wts
 
 
+def time_hub_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None, hub_edges: int = 200_000):
+    """A heavy real receiver: the conv workload's graph plus one more node that receives
+    hub_edges edges from random senders. Conv forward device times: the split forward on that
+    graph (the hub cut into 256-edge pieces), the plain forward on the workload's own graph,
+    and one launch of the plain forward on the hub graph (one warp sums the hub's edges)."""
+    import torch
+
+    import message_passing_gb300 as e3
+    from synth import STREAM_W, device_normal
+    from synth import workloads as W
+    t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
+    g = W.make_graph(wl, n_atoms=n_atoms)
+    x_np, _ = W.make_conv(wl, g, t.n_paths, edge_ids=np.zeros(0, np.int64))
+    N0, E0 = g.n_nodes, g.n_edges
+    rng = np.random.default_rng([wl.wid, 11])
+    hub_send = np.sort(rng.integers(0, N0, hub_edges)).astype(np.int32)
+    rowptr = np.concatenate([g.rowptr, [E0 + hub_edges]]).astype(np.int32)
+    sender = np.concatenate([g.sender, hub_send]).astype(np.int32)
+    x_np = np.concatenate([x_np, rng.standard_normal((1,) + x_np.shape[1:]).astype(x_np.dtype)])
+    vec = np.concatenate([g.vec, rng.standard_normal((hub_edges, 3))]).astype(np.float32)
+    N, E, Nq, P, D = N0 + 1, E0 + hub_edges, wl.mul, t.n_paths, t.D
+    xd = torch.from_numpy(x_np).to(dev)
+    rp, sd = torch.from_numpy(rowptr).to(dev), torch.from_numpy(sender).to(dev)
+    y = e3.sh_forward(torch.from_numpy(vec).to(dev), wl.sh_lmax)
+    wd = device_normal((E, P, Nq), (wl.wid, STREAM_W), W.weight_scale(wl, P), device=dev)
+    m = torch.empty((N, D, Nq), device=dev)
+    chunk = 256
+    ws = torch.empty(e3.load().e3gb_conv_forward_split_workspace_bytes(t.handle, N, E, chunk), dtype=torch.uint8,
+                     device=dev)
+    scale = N / E
+
+    def timed(fn, n):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        return _median([e[0].elapsed_time(e[1]) for e in ev[min(2, n - 1):]])
+
+    t_split = timed(lambda: e3.conv_forward_split(t, rp, sd, xd, y, wd, scale, chunk=chunk, out=m, workspace=ws,
+                                                  stream=stream), reps + 2)
+    m_split = m.clone()
+    t_plain_hub = timed(lambda: e3.conv_forward(t, rp, sd, xd, y, wd, scale, out=m, stream=stream), 1)
+    e3.check_device_status()
+    same_light = bool(torch.equal(m_split[:N0], m[:N0]))
+    rp0, sd0 = rp[:N0 + 1], sd[:E0]
+    m0 = torch.empty((N0, D, Nq), device=dev)
+    t_base = timed(lambda: e3.conv_forward(t, rp0, sd0, xd[:N0], y[:E0], wd[:E0], scale, out=m0, stream=stream),
+                   reps + 2)
+    e3.check_device_status()
+    del xd, wd, y, m, m0, ws, m_split
+    torch.cuda.empty_cache()
+    return {"workload": f"{wl.name} + one hub receiver of {hub_edges} edges (split forward, chunk {chunk})",
+            "dtype": "f32", "atoms": N0, "edges": E, "hub_edges": hub_edges,
+            "fwd_split_ms": t_split, "fwd_plain_ms_on_hub_graph": t_plain_hub,
+            "fwd_plain_ms_without_hub": t_base, "light_receivers_bitwise_equal": same_light,
+            "edges_per_s_split": E / (t_split / 1e3)}
+
+
 def time_radial_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None):
     """The radial form of the convolution step (e3j App. E.1, the edge scalars produced by a
     radial network; App. A.3 "Linear mixing" fused into message passing): SH + the radial
@@ -788,7 +848,8 @@ def run_ours(args):
                 ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
                                                    pad_frac=0.25, n_atoms=na)),
                 ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak)),
-                ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na))]
+                ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na)),
+                ("hub", lambda: time_hub_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na))]
         others = [f() for k, f in jobs if "all" in want or k in want]
         if "all" in want or "dbwd" in want:
             double_bwd = time_double_backward(W.WORKLOADS[4], dev, stream, 3, hbm_peak, n_atoms=args.dbwd_atoms)
@@ -842,7 +903,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload kernel timings")
     ap.add_argument("--workloads", default="all",
-                    help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,radial4,dbwd "
+                    help="comma list of per-workload timings: tp1,conv4,conv3,conv4bf16,conv5,pad,coo,radial4,hub,dbwd "
                          "(or all)")
     ap.add_argument("--dbwd-atoms", type=int, default=None, help="smaller double-backward case (profiling)")
     ap.add_argument("--workload-atoms", type=int, default=None,

@@ -207,7 +207,10 @@ e3gb_status e3gb_conv_forward(const e3gb_table *t, int64_t n_nodes, int64_t n_ed
  * a different (fixed) summation order. Arguments as e3gb_conv_forward, plus chunk >= 1 and a
  * device workspace of at least e3gb_conv_forward_split_workspace_bytes bytes (16-byte
  * aligned; contents on entry do not matter). E3GB_ERR_UNSUPPORTED for configurations with more
- * than 32 output rows. */
+ * than 32 output rows. Choosing chunk: each further piece is one warp's serial walk, so the
+ * pieces finish in about chunk x (one warp's time per edge) when they fit in one wave of
+ * warps; a chunk a few times the typical degree (256 for degree ~40) leaves ordinary
+ * receivers whole and gives a hub of 200,000 edges ~780 warps. */
 size_t e3gb_conv_forward_split_workspace_bytes(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,
                                                int32_t chunk);
 e3gb_status e3gb_conv_forward_split(const e3gb_table *t, int64_t n_nodes, int64_t n_edges,

@@ -386,7 +386,7 @@ def conv_forward(t: Table, rowptr, sender, x, y, w, scale: float, out=None, stre
     return m
 
 
-def conv_forward_split(t: Table, rowptr, sender, x, y, w, scale: float, chunk: int = 1024, out=None, workspace=None,
+def conv_forward_split(t: Table, rowptr, sender, x, y, w, scale: float, chunk: int = 256, out=None, workspace=None,
                        stream=None, pad_node: int = -1):
     """conv_forward with receivers of more than `chunk` edges cut into pieces summed by separate
     warps and added in piece order (deterministic); for graphs with heavy receivers."""

@@ -13,7 +13,7 @@ import torch
 
 import message_passing_gb300 as e3
 import oracle
-from gpu_util import TOL_F32, assert_close, to_dev, to_np
+from gpu_util import TOL_BF16, TOL_F32, assert_close, to_dev, to_np
 from synth import Graph
 
 pytestmark = pytest.mark.gpu
@@ -109,3 +109,34 @@ def test_split_forward_padding_and_small_chunks():
         assert e3.check_device_status() == 0
         assert torch.all(m[pad] == 0)
         assert_close(to_np(m), ref, TOL_F32, f"m (chunk {chunk})")
+
+
+@pytest.mark.parametrize("blocks", [[(0, 1), (1, -1)],              # plain bf16 forward
+                                    [(0, 1), (1, -1), (2, 1)]])     # pipelined bf16 forward
+def test_split_forward_heavy_receiver_bf16(blocks):
+    """bf16 storage, fp32 sums: a hub of 20,000 edges against the oracle on the same stored
+    bf16 inputs (harmonics included), and bitwise equal to the unsplit forward elsewhere."""
+    mul, L = 128, 3
+    t = e3.Table.create(blocks, mul, L, L)
+    ot = oracle.table(blocks, L, L)
+    g = _hub_graph(300, 20_000, 24, 9)
+    rng = np.random.default_rng(10)
+    bf = torch.bfloat16
+    xd = to_dev(rng.standard_normal((g.n_nodes, ot.d1, mul)).astype(np.float32), bf)
+    wd = to_dev((rng.standard_normal((g.n_edges, ot.n_paths, mul)) / np.sqrt(ot.n_paths)).astype(np.float32), bf)
+    v32 = g.vec.astype(np.float32)
+    yb = torch.from_numpy(oracle.sh(v32.astype(np.float64), L).astype(np.float32)).to(bf)
+    yd = yb.cuda()
+    rp, sd = to_dev(g.rowptr), to_dev(g.sender)
+    scale = g.n_nodes / g.n_edges
+    ms = e3.conv_forward_split(t, rp, sd, xd, yd, wd, scale, chunk=512)
+    m1 = e3.conv_forward(t, rp, sd, xd, yd, wd, scale)
+    torch.cuda.synchronize()
+    assert e3.check_device_status() == 0
+    light = torch.from_numpy(np.nonzero(np.diff(g.rowptr) <= 512)[0]).cuda()
+    assert torch.equal(ms[light], m1[light])
+    rcv = np.array([0, 17, 299])
+    ref = oracle.conv_forward(ot, g.rowptr, g.sender, to_np(xd), to_np(yb), to_np(wd), scale, receivers=rcv)
+    got = to_np(ms[torch.from_numpy(rcv).cuda()])
+    assert_close(got[1], ref[1], TOL_BF16, "m (hub)")
+    assert_close(got[[0, 2]], ref[[0, 2]], TOL_BF16, "m (neighbours)")
