@@ -431,7 +431,7 @@ def time_hub_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None,
     wd = device_normal((E, P, Nq), (wl.wid, STREAM_W), W.weight_scale(wl, P), device=dev)
     m = torch.empty((N, D, Nq), device=dev)
     chunk = 256
-    ws = torch.empty(e3.load().e3gb_conv_forward_split_workspace_bytes(t.handle, N, E, chunk), dtype=torch.uint8,
+    ws = torch.empty(e3.load().e3gb_conv_forward_split_workspace_bytes(t.handle, N, E, 64), dtype=torch.uint8,
                      device=dev)
     scale = N / E
 
@@ -444,6 +444,8 @@ def time_hub_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None,
         torch.cuda.synchronize()
         return _median([e[0].elapsed_time(e[1]) for e in ev[min(2, n - 1):]])
 
+    sweep = {c: timed(lambda: e3.conv_forward_split(t, rp, sd, xd, y, wd, scale, chunk=c, out=m, workspace=ws,
+                                                    stream=stream), reps + 2) for c in (64, 1024)}
     t_split = timed(lambda: e3.conv_forward_split(t, rp, sd, xd, y, wd, scale, chunk=chunk, out=m, workspace=ws,
                                                   stream=stream), reps + 2)
     m_split = m.clone()
@@ -459,7 +461,8 @@ def time_hub_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=None,
     torch.cuda.empty_cache()
     return {"workload": f"{wl.name} + one hub receiver of {hub_edges} edges (split forward, chunk {chunk})",
             "dtype": "f32", "atoms": N0, "edges": E, "hub_edges": hub_edges,
-            "fwd_split_ms": t_split, "fwd_plain_ms_on_hub_graph": t_plain_hub,
+            "fwd_split_ms": t_split, "fwd_split_ms_by_chunk": {"64": sweep[64], "256": t_split, "1024": sweep[1024]},
+            "fwd_plain_ms_on_hub_graph": t_plain_hub,
             "fwd_plain_ms_without_hub": t_base, "light_receivers_bitwise_equal": same_light,
             "edges_per_s_split": E / (t_split / 1e3)}
 

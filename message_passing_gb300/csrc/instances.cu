@@ -7,6 +7,7 @@
 #include "conv_pipe.cuh"
 #include "conv_pipe_dd.cuh"
 #include "conv_slots.cuh"
+#include "conv_split.cuh"
 #include "kernels.cuh"
 
 #include <type_traits>
@@ -269,9 +270,9 @@ cudaError_t conv_fwd_pieces(int64_t N, int64_t E, int Nq, const int32_t* rowptr,
                                   partials, err);
         st = cudaGetLastError();
         if (st != cudaSuccess) return st;
-        const int64_t nb = (N + 7) / 8;
-        conv_pieces_combine_kernel<<<int(nb < 65535 ? nb : 65535), 256, 0, s>>>(N, int64_t(Cfg::D) * Nq, ptr, partials,
-                                                                                 scale, (float*)m);
+        const int64_t row = int64_t(Cfg::D) * Nq;
+        const dim3 cgrid(unsigned(N < 2048 ? N : 2048), unsigned((row + 255) / 256));
+        conv_pieces_combine_kernel<<<cgrid, 256, 0, s>>>(N, row, ptr, partials, scale, (float*)m);
         return cudaGetLastError();
     }
 }

@@ -108,3 +108,13 @@ def test_no_records_and_determinism():
     a = [e3.coo_tp_backward(rec_d, c_d, x, y, w, dz) for _ in range(3)]
     for u in a[1:]:
         assert all(torch.equal(p, q) for p, q in zip(a[0], u))
+
+
+@pytest.mark.parametrize("n", [8192, 8193])
+def test_record_count_at_the_sorted_plan_limit(n):
+    """8,192 records take the sorted-plan kernels, 8,193 the general ones: both against the
+    oracle, with repeats and random order."""
+    r = np.random.default_rng(n)
+    d1, d2, P, D = 6, 5, 3, 7
+    recs = np.stack([r.integers(0, D, n), r.integers(0, d1, n), r.integers(0, d2, n), r.integers(0, P, n)], 1)
+    _check(recs, r.standard_normal(n) / np.sqrt(n), (d1, d2, P, D), 16, torch.float32, R=97, seed=n)
