@@ -141,3 +141,102 @@ def test_sharded_conv_gloo():
         p.join(timeout=120)
         assert p.exitcode == 0
     assert ok
+
+
+def _graph(seed, N=150, deg_max=9):
+    """Receiver-sorted CSR of a random graph (senders anywhere, ascending per receiver)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    d = rng.integers(0, deg_max, N)
+    d[rng.integers(0, N)] = 40   # one busier receiver
+    rowptr = np.zeros(N + 1, np.int64)
+    np.cumsum(d, out=rowptr[1:])
+    sender = np.concatenate([np.sort(rng.integers(0, N, k)) for k in d]).astype(np.int64)
+    return rowptr, sender
+
+
+def test_halo_partition_local_graphs():
+    """Each rank's local graph is its owned receivers' edges with senders renamed into the
+    local index space (owned nodes, then the halo in ascending id); halo nodes have empty
+    segments; the cuts cover the nodes and balance the edges to within one receiver."""
+    import numpy as np
+    from message_passing_gb300.halo import HaloPartition
+    for seed in range(6):
+        rowptr, sender = _graph(seed)
+        N, E = rowptr.shape[0] - 1, int(rowptr[-1])
+        dmax = int(np.diff(rowptr).max())
+        for world in (1, 2, 3, 5):
+            parts = [HaloPartition(rowptr, sender, world, r) for r in range(world)]
+            assert parts[0].n0 == 0 and parts[-1].n1 == N
+            for a, b in zip(parts[:-1], parts[1:]):
+                assert a.n1 == b.n0 and a.e1 == b.e0
+            for p in parts:
+                assert abs((p.e1 - p.e0) - E / world) <= dmax
+                assert p.rowptr.shape[0] == p.n_local + 1 and p.rowptr[-1] == p.e1 - p.e0
+                assert np.all(p.rowptr[p.n_owned:] == p.e1 - p.e0)   # halo nodes receive nothing
+                lut = np.concatenate([np.arange(p.n0, p.n1), p.halo])   # local id -> global id
+                assert np.array_equal(lut[p.sender], sender[p.e0:p.e1])
+                out = sender[p.e0:p.e1]
+                out = out[(out < p.n0) | (out >= p.n1)]
+                assert np.array_equal(p.halo, np.unique(out))
+                assert np.array_equal(p.rowptr[:p.n_owned + 1], rowptr[p.n0:p.n1 + 1] - p.e0)
+
+
+def _halo_worker(rank, world, port, q):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from message_passing_gb300.halo import HaloPartition
+    blocks, L, mul, scale = [(0, 1), (1, -1)], 2, 4, 0.3
+    ot = oracle.table(blocks, L, L)
+    rowptr, sender = _graph(21)
+    N, E = rowptr.shape[0] - 1, int(rowptr[-1])
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((N, ot.d1, mul))
+    y = oracle.sh(rng.standard_normal((E, 3)), L)
+    w = rng.standard_normal((E, ot.n_paths, mul))
+    dm = rng.standard_normal((N, ot.D, mul))
+    p = HaloPartition(rowptr, sender, world, rank).setup()
+    # forward: halo rows from their owners, then the local convolution (oracle as the compute)
+    x_local = p.gather_halo(torch.from_numpy(x[p.n0:p.n1].copy())).numpy()
+    yl, wl = y[p.e0:p.e1], w[p.e0:p.e1]
+    m = oracle.conv_forward(ot, p.rowptr, p.sender, x_local, yl, wl, scale)[:p.n_owned]
+    # backward: local dx partials (owned and halo senders) sent back to their owners
+    dm_local = np.concatenate([dm[p.n0:p.n1], np.zeros((p.n_local - p.n_owned, ot.D, mul))])
+    dx_local = oracle.conv_backward_dx(ot, p.rowptr, p.sender, yl, wl, dm_local, scale, Nq=mul)
+    dx = p.scatter_halo_grad(torch.from_numpy(dx_local)).numpy()
+    dy, dw = oracle.conv_backward_edges(ot, p.rowptr, p.sender, x_local, yl, wl, dm_local, scale)
+    parts = [None] * world
+    dist.all_gather_object(parts, (p.n0, m, dx, dy, dw))   # collected for the check only
+    if rank == 0:
+        parts.sort(key=lambda t: t[0])
+        got = [np.concatenate([t[i] for t in parts]) for i in (1, 2, 3, 4)]
+        want_m = oracle.conv_forward(ot, rowptr, sender, x, y, w, scale)
+        want_dx = oracle.conv_backward_dx(ot, rowptr, sender, y, w, dm, scale, Nq=mul)
+        want_dy, want_dw = oracle.conv_backward_edges(ot, rowptr, sender, x, y, w, dm, scale)
+        ok = (np.array_equal(got[0], want_m) and np.array_equal(got[2], want_dy) and np.array_equal(got[3], want_dw)
+              and np.allclose(got[1], want_dx, rtol=0, atol=1e-12 * np.abs(want_dx).max()))
+        q.put(bool(ok))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_halo_conv_gloo(world):
+    """One graph over gloo ranks: each convolves its receivers after the halo gather and
+    returns the halo senders' dx partials to their owners. Messages, dy and dw equal the whole
+    graph's bitwise; dx to rounding (its sums are split between ranks)."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_halo_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    ok = q.get(timeout=240)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert ok
