@@ -113,8 +113,10 @@ def test_no_records_and_determinism():
 @pytest.mark.parametrize("n", [8192, 8193])
 def test_record_count_at_the_sorted_plan_limit(n):
     """8,192 records take the sorted-plan kernels, 8,193 the general ones: both against the
-    oracle, with repeats and random order."""
+    oracle, with repeats and random order. 64 rows of every index, so that each output (z, dx,
+    dy, dw) sums ~128 records (a CG list sums tens): the fp32 rounding of a sum grows with its
+    length, and 1,000-term sums of random-signed terms reach the 1e-5 RMS bound by themselves."""
     r = np.random.default_rng(n)
-    d1, d2, P, D = 6, 5, 3, 7
+    d1, d2, P, D = 64, 64, 64, 64
     recs = np.stack([r.integers(0, D, n), r.integers(0, d1, n), r.integers(0, d2, n), r.integers(0, P, n)], 1)
     _check(recs, r.standard_normal(n) / np.sqrt(n), (d1, d2, P, D), 16, torch.float32, R=97, seed=n)
