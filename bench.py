@@ -13,7 +13,7 @@ public API with host buffers: pinned host -> device copies of the step's inputs 
 device -> host copies of all outputs inside the timed region (consecutive steps overlap their
 copies and compute on three streams with two device buffer sets).
 
-Profiling options shrink single parts of the run (--atoms for the main step, --tp-rows,
+Profiling options shrink single parts of the run (--atoms for the main step, --tp-rows, --coo-rows,
 --workload-atoms for every conv workload's box, --dbwd-atoms, --workloads to pick timings).
 
 Throughput accounting follows "e3j ...", Sec. 3 Eq. (9): (bytes of inputs + outputs) /
@@ -533,9 +533,9 @@ def time_radial_workload(wl, dev, stream, reps: int, hbm_peak: float, n_atoms=No
     return res
 
 
-def time_coo_tp(wl, dev, stream, reps: int, hbm_peak: float):
+def time_coo_tp(wl, dev, stream, reps: int, hbm_peak: float, rows=None):
     """The generic COO-coefficient tensor product with the table's CG records, beside the
-    compile-time kernels, on a row workload (fp32)."""
+    compile-time kernels, on a row workload (fp32); rows: fewer rows (profiling)."""
     import torch
 
     import message_passing_gb300 as e3
@@ -543,7 +543,7 @@ def time_coo_tp(wl, dev, stream, reps: int, hbm_peak: float):
     t = e3.Table.create(wl.blocks, wl.mul, wl.sh_lmax, wl.out_lmax)
     rec, coef = t.coo_records()
     rec_d, coef_d = torch.from_numpy(rec).to(dev), torch.from_numpy(coef).to(dev)
-    u, x, ww = W.make_tp(wl, t.n_paths)
+    u, x, ww = W.make_tp(wl, t.n_paths, rows=rows)
     R = x.shape[0]
     xd, wd = torch.from_numpy(x).to(dev), torch.from_numpy(ww).to(dev)
     y = e3.sh_forward(torch.from_numpy(u.astype(np.float32)).to(dev), wl.sh_lmax)
@@ -850,7 +850,7 @@ def run_ours(args):
                                                      n_atoms=na)),
                 ("pad", lambda: time_conv_workload(W.WORKLOADS[4], torch.float32, dev, stream, 5, hbm_peak,
                                                    pad_frac=0.25, n_atoms=na)),
-                ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak)),
+                ("coo", lambda: time_coo_tp(W.WORKLOADS[2], dev, stream, 5, hbm_peak, rows=args.coo_rows)),
                 ("radial4", lambda: time_radial_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na)),
                 ("hub", lambda: time_hub_workload(W.WORKLOADS[4], dev, stream, 5, hbm_peak, n_atoms=na))]
         others = [f() for k, f in jobs if "all" in want or k in want]
@@ -899,6 +899,7 @@ def main():
     ap.add_argument("--order", choices=["cell", "draw"], default="cell")
     ap.add_argument("--atoms", type=int, default=None, help="smaller conv workload (profiling)")
     ap.add_argument("--tp-rows", type=int, default=None, help="smaller TP workload (profiling)")
+    ap.add_argument("--coo-rows", type=int, default=None, help="smaller COO workload (profiling)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--ref-receivers", type=int, default=24)
     ap.add_argument("--no-tp", action="store_true")

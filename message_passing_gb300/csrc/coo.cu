@@ -218,7 +218,7 @@ __device__ bool coo_build_plan(bool bwd, int nrec, const int4* __restrict__ rec,
 }
 
 template <class T, int V>
-__global__ void __launch_bounds__(256, 1) coo_plan_forward_kernel(int64_t R, int d1, int d2, int D, int P, int Nq,
+__global__ void __launch_bounds__(256, 4) coo_plan_forward_kernel(int64_t R, int d1, int d2, int D, int P, int Nq,
                                                                int nrec, const int4* __restrict__ rec,
                                                                const float* __restrict__ coef,
                                                                const T* __restrict__ x, const T* __restrict__ y,
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(256, 1) coo_plan_forward_kernel(int64_t R, int
 }
 
 template <class T, int V>
-__global__ void __launch_bounds__(256, 1) coo_plan_backward_kernel(int64_t R, int d1, int d2, int D, int P, int Nq,
+__global__ void __launch_bounds__(256, 3) coo_plan_backward_kernel(int64_t R, int d1, int d2, int D, int P, int Nq,
                                                                    int nrec, const int4* __restrict__ rec,
                                                                    const float* __restrict__ coef,
                                                                    const T* __restrict__ x, const T* __restrict__ y,
