@@ -13,7 +13,9 @@ Local index space of rank r: its owned nodes first (global id - n0), then its ha
 ascending global id. The local graph has one empty receiver segment per halo node, so local
 node arrays have n_owned + n_halo rows and the library's calls take it as any other graph.
 The exchanges go through torch.distributed point-to-point operations (NCCL between GPUs,
-gloo on CPU); the order of every sum is fixed, so results are deterministic.
+gloo on CPU); the order of every sum is fixed, so results are deterministic. A padding node
+(e3j, Sec. 4) keeps its role on every rank: pass local_index([pad]) as the calls' pad_node
+(its owner's local id, a halo id where it sends into other ranks, -1 elsewhere).
 """
 from __future__ import annotations
 
@@ -73,6 +75,19 @@ class HaloPartition:
         self.recv_pos = {r: self.n_owned + np.nonzero(owner == r)[0] for r in range(world) if r != rank}
         self._need = {r: self.halo[owner == r] for r in range(world) if r != rank}
         self.send_pos = None
+
+    def local_index(self, global_ids):
+        """Local ids of global node ids (owned nodes, then halo nodes); -1 where a node is
+        neither (for example, to pass a padding node's id to the library's pad_node)."""
+        g = np.asarray(global_ids, dtype=np.int64)
+        out = np.full(g.shape, -1, dtype=np.int64)
+        own = (g >= self.n0) & (g < self.n1)
+        out[own] = g[own] - self.n0
+        pos = np.searchsorted(self.halo, g)
+        hit = ~own & (pos < self.halo.shape[0])
+        hit[hit] = self.halo[pos[hit]] == g[hit]
+        out[hit] = self.n_owned + pos[hit]
+        return out
 
     def setup(self, group=None):
         """Exchange the halo lists once: afterwards send_pos[r] holds the local (owned)

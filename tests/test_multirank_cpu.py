@@ -240,3 +240,19 @@ def test_halo_conv_gloo(world):
         p.join(timeout=120)
         assert p.exitcode == 0
     assert ok
+
+
+def test_halo_local_index():
+    """local_index maps owned and halo nodes into the local index space, -1 elsewhere."""
+    import numpy as np
+    from message_passing_gb300.halo import HaloPartition
+    rowptr, sender = _graph(5)
+    N = rowptr.shape[0] - 1
+    for world in (2, 4):
+        for r in range(world):
+            p = HaloPartition(rowptr, sender, world, r)
+            lut = np.concatenate([np.arange(p.n0, p.n1), p.halo])
+            li = p.local_index(np.arange(N))
+            assert np.array_equal(np.nonzero(li >= 0)[0], np.sort(lut))
+            assert np.array_equal(lut[li[li >= 0]], np.nonzero(li >= 0)[0])
+            assert np.array_equal(p.local_index(lut), np.arange(p.n_local))
