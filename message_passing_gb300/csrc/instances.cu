@@ -115,9 +115,12 @@ bool conv_dbwd_pipe(int64_t N, int64_t E, int Nq, const int32_t* rowptr, const i
 template <class T>
 cudaError_t tp_fwd(int64_t R, int Nq, const void* x, const void* y, const void* w, void* z, cudaStream_t s) {
     auto k = vec_for(Nq) == 4 ? tp_forward_kernel<Cfg, T, 4> : tp_forward_kernel<Cfg, T, 1>;
-    const int grid = grid_for((const void*)k, kBlock, rows_per_block(Nq), R);
+    // 4 channels per lane: 12 warps per block (at <= 168 registers, three per scheduler), which
+    // measured 11% faster than 8 on the 200k-row workload; one channel per lane: 8
+    const int blk = vec_for(Nq) == 4 ? 384 : kBlock;
+    const int grid = grid_for((const void*)k, blk, (blk / 32) * (32 / (Nq / vec_for(Nq))), R);
     if (grid == 0) return cudaSuccess;
-    k<<<grid, kBlock, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (float*)z);
+    k<<<grid, blk, 0, s>>>(R, Nq, (const T*)x, (const T*)y, (const T*)w, (float*)z);
     return cudaGetLastError();
 }
 

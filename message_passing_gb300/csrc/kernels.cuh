@@ -206,7 +206,7 @@ __device__ __forceinline__ Lanes lanes_for(int Nq) {
 // TP forward on rows: output block by output block, so only one block's accumulators live.
 // ------------------------------------------------------------------------------------------
 template <class Cfg, class T, int V>
-__global__ void __launch_bounds__(256) tp_forward_kernel(int64_t R, int Nq, const T* __restrict__ x,
+__global__ void __launch_bounds__(384) tp_forward_kernel(int64_t R, int Nq, const T* __restrict__ x,
                                                          const T* __restrict__ y, const T* __restrict__ w,
                                                          float* __restrict__ z) {
     const Lanes L = lanes_for<V>(Nq);
